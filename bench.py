@@ -1,0 +1,509 @@
+"""Benchmark of the CSA2 layer step on GB300 (prints one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|hierarchical|ragged]
+    python bench.py --impl reference ...      # the CPU oracle on a bounded sample
+
+A step is one pass of the layer group over one batch of synthetic input,
+inputs resident in HBM: for the default decode workload (32 sequences x one
+token over a 131,072-token context, Full mode) that is window pack, index
+scoring of every visible entry, Top-512 and sparse attention.  L2 is flushed
+(a 512 MB write) before every timed step.  Under torchrun each rank runs an
+independent replica on its own GPU (weak scaling, no collective on the data
+path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 sparse-attn tokens/s (decode@128K, prefill@64K); % HBM/TC roofline"
+FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------------
+# workload bytes / flops (algorithmic: what the method must move or compute)
+
+def algorithmic(wl):
+    """Per-step algorithmic work of the workload's hot path and its dominant kernel."""
+    d, Di, K, W, Hq = wl.d, wl.Di, wl.K, wl.W, wl.Hq
+    entry_bytes = d // 2 + d // 16                       # 288 B MXFP4 entry (d = 512)
+    idx_elt = 2 if wl.idx_dtype == "bf16" else 4
+    scan = 0          # indexer keys read by Full layers
+    pooled = 0        # indexer keys read by Reindex layers
+    gathered = 0      # selected MXFP4 entries gathered by attention
+    attn_flops = 0
+    idx_flops = 0
+    for b in range(wl.B):
+        for i in range(wl.Tq):
+            t = wl.t_first[b] + i
+            nv = max(0, min(wl.entries_after(b), (t + 1) // 4))
+            nk = min(K, nv)
+            nwin = min(W, t + 1)
+            for mode in wl.layers:
+                if mode == "F":
+                    scan += nv * Di * idx_elt
+                    idx_flops += 2 * nv * wl.Hi * Di
+                elif mode == "X":
+                    npos = min(nv, wl.pool_blocks * wl.pool_block)
+                    pooled += npos * Di * idx_elt
+                    idx_flops += 2 * npos * wl.Hi * Di
+                gathered += nk * entry_bytes
+                attn_flops += 4 * Hq * d * (nk + nwin)
+    compress_flops = 0
+    if wl.H is not None:
+        compress_flops = 2 * sum(wl.new_entries(b) for b in range(wl.B)) * 4 * wl.H * (d + Di)
+    return {"scan_bytes": scan, "pooled_bytes": pooled, "gathered_bytes": gathered,
+            "step_bytes": scan + pooled + gathered, "attn_flops": attn_flops, "index_flops": idx_flops,
+            "compress_flops": compress_flops}
+
+
+def make_workload(name):
+    from csa2_inputs import workloads as WL
+    return WL.ALL[name]()
+
+
+# ---------------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        self.lines = []
+        if self.proc:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# ncu traffic figure committed under profiles/ (used only while the kernel is unchanged)
+
+def kernel_source_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def committed_traffic(profile_md, src_path):
+    try:
+        text = open(profile_md).read()
+    except OSError:
+        return None
+    m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+    if not (m_sha and m_tr) or m_sha.group(1) != kernel_source_hash(src_path):
+        return None
+    return float(m_tr.group(1))
+
+
+# ---------------------------------------------------------------------------------
+# GPU arm
+
+def run_gpu(args, rank, world, dist):
+    import torch
+
+    from compressed_sparse_attention_05_gb300 import abi, build, harness
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.workload)
+    wl.seed += 1000 * rank                       # an independent replica per rank
+    alg = algorithmic(wl)
+    g = harness.LayerGroup(wl, f"cuda:{local}")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for w in range(args.warmup):
+        flush.fill_(w & 255)
+        g.step()
+    torch.cuda.synchronize()
+    assert abi.csa2_get_status() == 0
+
+    # ---- headline: K steps, inputs resident, L2 flushed before each
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    n0 = abi.csa2_launch_count()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush.fill_(k & 255)
+            ev[k][0].record(stream)
+            g.step()
+            ev[k][1].record(stream)
+        barrier()
+    launches = abi.csa2_launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = sum(step_ms) / args.steps
+    ms_all = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_all = float(t)
+
+    # ---- dominant kernel, timed alone on the same stream through its own entry point
+    kern = time_dominant_kernel(args, g, wl, flush, stream)
+
+    # ---- end to end through the public call with host buffers
+    e2e = time_e2e(args, g, flush, stream, dist)
+
+    status = abi.csa2_get_status()
+    if rank != 0:
+        return
+    tokens = wl.B * wl.Tq
+    value = world * tokens / (ms_all / 1e3)
+    peaks = load_peaks()
+    roof = roofline(wl, alg, kern, peaks)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": tokens,
+                   "layers": "".join(wl.layers), "K": wl.K, "Hq": wl.Hq, "d": wl.d, "W": wl.W,
+                   "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": "MXFP4 288 B/entry, 64-entry pages",
+                   "l2": "flushed before every timed step (512 MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "step_roofline": step_roofline(wl, alg, ms, peaks),
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "status_word": status,
+        "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def time_dominant_kernel(args, g, wl, flush, stream):
+    """Average duration of the dominant kernel of the step, launched as in the step."""
+    import torch
+
+    from compressed_sparse_attention_05_gb300 import abi
+
+    n = max(3, min(args.steps, 200))
+    if wl.H is None:   # decode-type workloads: the Full layer's indexer scan
+        stride = g.max_entries
+        scores = torch.empty(wl.B * wl.Tq, stride, dtype=torch.float32, device=flush.device)
+        fn = lambda: abi.csa2_index_scores(g.dims(), g.cache(), g.idx_q[0], g.idx_w[0], g.q_pos, scores)  # noqa
+        name = "k_index_scores_mma"
+    else:              # prefill: attention of the Full layer
+        fn = lambda: abi.csa2_sparse_attn(g.dims(), g.cache(), g.window(0), g.Q[0], g.q_pos, g.idx[0],  # noqa
+                                          g.cnt[0], 1.0 / math.sqrt(wl.d), g.O[0], g.lse[0])
+        name = "k_sparse_attn"
+    fn()
+    tot = 0.0
+    for k in range(n):
+        flush.fill_(k & 255)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return {"name": name, "ms": tot / n, "launches_timed": n}
+
+
+def time_e2e(args, g, flush, stream, dist):
+    """Same step through the public call, per-step inputs copied from pinned host memory
+    before it and the attention outputs read back after it, all inside the timed region."""
+    import torch
+
+    ins = g.step_inputs()
+    outs = g.step_outputs()
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = sum(t.numel() * t.element_size() for t in outs)
+    n = max(3, min(args.steps, 200))
+    tot = 0.0
+    if dist is not None:
+        dist.barrier()
+    for k in range(n):
+        flush.fill_(k & 255)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for d_, h in zip(ins, h_in):
+            d_.copy_(h, non_blocking=True)
+        g.step()
+        for h, d_ in zip(h_out, outs):
+            h.copy_(d_, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    ms = tot / n
+    world = dist.get_world_size() if dist is not None else 1
+    if dist is not None:
+        t = torch.tensor([ms], device=flush.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t)
+    wl = g.wl
+    return {"value": world * wl.B * wl.Tq / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+def load_peaks():
+    try:
+        p = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def roofline(wl, alg, kern, peaks):
+    src = os.path.join(ROOT, "compressed_sparse_attention_05_gb300", "csrc")
+    if kern["name"] == "k_index_scores_mma":
+        bytes_ = alg["scan_bytes"]
+        achieved = bytes_ / (kern["ms"] / 1e3) / 1e9
+        traffic = committed_traffic(os.path.join(ROOT, "profiles", f"index_scores_{wl.name}.md"),
+                                    os.path.join(src, "indexer.cu"))
+        return {"bound": "hbm", "kernel": kern["name"], "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": bytes_, "kernel_ms": kern["ms"],
+                "peak_source": peaks["source"] + " (hbm copy)"}
+    flops = alg["attn_flops"]
+    achieved = flops / (kern["ms"] / 1e3) / 1e12
+    traffic = committed_traffic(os.path.join(ROOT, "profiles", f"sparse_attn_{wl.name}.md"),
+                                os.path.join(src, "attention.cu"))
+    return {"bound": "tensor", "kernel": kern["name"], "achieved": achieved, "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+            "algorithmic_flops_per_launch": flops, "kernel_ms": kern["ms"],
+            "peak_source": peaks["source"] + " (bf16 burst)"}
+
+
+def step_roofline(wl, alg, ms, peaks):
+    t_bytes = alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_flops = (alg["attn_flops"] + alg["index_flops"] + alg["compress_flops"]) / (peaks["bf16_tflops"] * 1e12)
+    bound = max(t_bytes, t_flops)
+    return {"bound": "hbm" if t_bytes >= t_flops else "tensor", "algorithmic_bytes": alg["step_bytes"],
+            "algorithmic_flops": alg["attn_flops"] + alg["index_flops"] + alg["compress_flops"],
+            "ideal_ms": bound * 1e3, "frac": bound * 1e3 / ms}
+
+
+# ---------------------------------------------------------------------------------
+# the CPU oracle on a bounded sample
+
+def cpu_baseline(workload, seconds):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-worker", "--workload", workload,
+           "--cpu-seconds", str(seconds)]
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 20 * seconds))
+    if r.returncode != 0:
+        return {"error": r.stderr[-500:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_worker(workload, seconds):
+    """Times the oracle's arithmetic for whole query tokens of the workload (inputs and
+    cached state prepared outside the timer), single-threaded."""
+    import numpy as np
+    import torch
+
+    torch.set_num_threads(1)
+    from oracle import attention as A
+    from oracle import formats as F
+    from oracle import indexer as I
+    from oracle import layer as OL
+
+    wl = make_workload(workload)
+    tau = 1.0 / math.sqrt(wl.d)
+    # the sample: one sequence (the median-length one), its query tokens prepared once
+    lens = [wl.entries_before(b) for b in range(wl.B)]
+    b = sorted(range(wl.B), key=lambda x: lens[x])[wl.B // 2]
+    st = OL.SequenceState(wl, b)
+    Kall = st.indexer_keys()
+    prepared = []
+    for i in ([0] if wl.Tq == 1 else [0, wl.Tq // 2, wl.Tq - 1]):
+        t = wl.t_first[b] + i
+        nv = I.n_visible(Kall.shape[0], t)
+        L = len(wl.layers)
+        qs = [(wl.idx_q_row(l, b, i).double().numpy(), wl.idx_w_row(l, b, i).double().numpy()) for l in range(L)]
+        Qs = [wl.q_row(l, b, i).double().numpy() for l in range(L)]
+        win_pos = A.window_positions(t, wl.W)
+        win_lat = [wl.swa_latent(l, b, torch.from_numpy(win_pos)).numpy() for l in range(L)]
+        # cached state: packed rows of every entry the schedule can gather (the Full
+        # selection and, for the pooled indexer, every pooled position)
+        sc = I.index_scores(qs[0][0], qs[0][1], Kall[:nv])
+        cand = [I.topk(sc, wl.K)]
+        if wl.hierarchical:
+            cand.append(I.pool_positions(I.block_pool(sc, wl.pool_blocks, wl.pool_block), nv, wl.pool_block))
+        cand = np.unique(np.concatenate(cand))
+        c, s = st.packed_rows(cand)
+        prepared.append((nv, qs, Qs, win_lat, cand, c, s))
+
+    def one_token(nv, qs, Qs, win_lat, cand, c, s):
+        prev = None
+        pool_t = None
+        for l, mode in enumerate(wl.layers):
+            if mode == "F":
+                sc = I.index_scores(qs[l][0], qs[l][1], Kall[:nv])
+                idx = I.topk(sc, wl.K)
+                if wl.hierarchical:
+                    pool_t = I.block_pool(sc, wl.pool_blocks, wl.pool_block)
+            elif mode == "X":
+                pos = I.pool_positions(pool_t, nv, wl.pool_block)
+                idx = pos[I.topk(I.index_scores(qs[l][0], qs[l][1], Kall[pos]), wl.K)]
+            else:
+                idx = prev
+            prev = idx
+            rows = np.searchsorted(cand, idx)
+            kv = F.mxfp4_unpack(c[rows], s[rows])
+            wc, ws = F.fp8_pack(win_lat[l])
+            A.sparse_attention(Qs[l], kv, F.fp8_unpack_bf16(wc, ws), tau)
+
+    t_tot, tokens = 0.0, 0
+    while t_tot < seconds:
+        for p in prepared:
+            t0 = time.perf_counter()
+            one_token(*p)
+            t_tot += time.perf_counter() - t0
+            tokens += 1
+    per_token = t_tot / max(tokens, 1)
+    # prefill: the step also compresses the chunk; time the oracle's compression once
+    extra = ""
+    if wl.H is not None:
+        from oracle import compress as Cm
+        st = OL.SequenceState(wl, 0)
+        hid = st.wl.hidden()[0].double().numpy()
+        W = st.wl.w_compress().double().numpy()
+        Wi = st.wl.w_index().double().numpy()
+        t0 = time.perf_counter()
+        Cm.compress_pack(hid, W, st.gamma, wl.eps, wl.r, wl.rope_base, st.n_before, W_idx=Wi)
+        t_comp = time.perf_counter() - t0
+        step_s = t_comp + per_token * wl.Tq
+        extra = f"; compression of the {wl.n_new}-token chunk timed once ({t_comp:.2f} s)"
+    else:
+        step_s = per_token * wl.Tq * wl.B
+    value = wl.B * wl.Tq / step_s
+    print(json.dumps({"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                      "sample": f"{tokens} query tokens of {wl.name} through all {len(wl.layers)} layer(s), "
+                                f"{t_tot:.1f} s of single-thread float64 numpy, scaled to the "
+                                f"{wl.B * wl.Tq}-token step{extra}",
+                      "seconds_per_token": per_token}))
+
+
+# ---------------------------------------------------------------------------------
+# reference arm: the oracle as it stands, timed on the host cores
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    steps = []
+    last = None
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline(args.workload, args.ref_seconds)
+        if "error" in r:
+            print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " + r["error"][-200:]}))
+            return
+        if k >= args.warmup:
+            steps.append(r["value"])
+        last = r
+    value = statistics.median(steps)
+    wl = make_workload(args.workload)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B * wl.Tq / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
+                         "sample": last["sample"]},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "hierarchical", "ragged"])
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=5.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-worker", action="store_true")
+    args = ap.parse_args()
+    if args.cpu_worker:
+        cpu_worker(args.workload, args.cpu_seconds)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+            return
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,284 @@
+// Gathered sparse MQA attention over the selected compressed entries plus
+// the FP8 sliding window.  "DeepSeek-V4.1 架构解析" §02 (fewer KV heads, attend
+// over the Top-K) and §03 (FP4 main KV dequantised before the matmul; SWA
+// kept in FP8, the last 128 raw tokens).  Head layout, key set and softmax:
+// reading R11 of include/csa2.h.
+//
+// One CTA per (query token, group of 16 heads), 4 warps.  Per 64-key tile:
+// gather + dequantise the keys into shared memory as bf16 (MXFP4 entries are
+// exact in bf16; window rows are bf16(e4m3 * scale)), S = Q K^T on tensor
+// cores (m16n8k16, each warp 16 keys), online softmax in fp32 (exp2 domain),
+// then O += P V with each warp owning a quarter of the value channels.
+// K = V: the same shared-memory tile feeds both products.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+constexpr int kAttnThreads = 128;
+constexpr int kTK = 64;       // keys per tile
+constexpr int kHG = 16;       // heads per CTA
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int D>
+struct AttnSmem {
+  static constexpr int QS = D + 8;     // row stride (elements) of Q and K tiles
+  static constexpr int PS = kTK + 8;   // row stride of P
+  uint16_t q[kHG * QS];
+  uint16_t k[kTK * QS];
+  float s[kHG * kTK];
+  uint16_t p[kHG * PS];
+  int64_t key_src[kTK];                // >= 0 main-KV slot; <= -2 window row (-2 - r); -1 none
+  float m[kHG], l[kHG], alpha[kHG];
+};
+
+// Dequantise one 16-channel group of a key into 16 bf16 in shared memory.
+template <int D>
+__device__ __forceinline__ void dequant_group(const AttnArgs& a, int b, int64_t src, int grp,
+                                              uint16_t* dst) {
+  uint32_t w[8];
+  if (src >= 0) {
+    const uint2 c = *reinterpret_cast<const uint2*>(a.kv_codes + src * (D / 2) + grp * 8);
+    const float sc = e4m3_to_f32(a.kv_scales[src * (D / 16) + grp]);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t word = i < 4 ? c.x : c.y;
+      const int sh = (i & 3) * 8;
+      const float lo = bf16_bits_to_f32(e2m1_to_bf16_bits((word >> sh) & 0xFu)) * sc;
+      const float hi = bf16_bits_to_f32(e2m1_to_bf16_bits((word >> (sh + 4)) & 0xFu)) * sc;
+      w[i] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact
+    }
+  } else if (src <= -2) {
+    const int64_t wr = (int64_t)b * a.swa_cap + (-2 - src);
+    const uint4 c = *reinterpret_cast<const uint4*>(a.swa_codes + wr * D + grp * 16);
+    const float sc = a.swa_scales[wr];
+    const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t word = cw[i >> 1];
+      const int sh = (i & 1) * 16;
+      const float lo = e4m3_to_f32((word >> sh) & 0xFFu) * sc;
+      const float hi = e4m3_to_f32((word >> (sh + 8)) & 0xFFu) * sc;
+      w[i] = f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = 0;
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads)
+k_sparse_attn(AttnArgs a, uint32_t* status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  AttnSmem<D>& sm = *reinterpret_cast<AttnSmem<D>*>(smem_raw);
+  constexpr int QS = AttnSmem<D>::QS, PS = AttnSmem<D>::PS;
+  constexpr int NT = D / 32;           // 8-wide value n-tiles per warp (D/4 channels)
+  const int64_t row = blockIdx.y;
+  const int hg = blockIdx.x;
+  const int b = (int)(row / a.Tq);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  const int t = a.q_pos[row];
+  const int nv = n_visible(a.n_entries[b], t);  // only bounds the indices checked below
+  int n_sel = a.cnt[row];
+  if (n_sel < 0 || n_sel > a.K) {
+    if (tid == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    n_sel = n_sel < 0 ? 0 : a.K;
+  }
+  const int pos0 = a.swa_cap > 0 ? a.swa_pos0[b] : 0;
+  const int w_lo = max(max(0, t - a.W + 1), pos0);
+  const int w_hi = min(t, pos0 + a.swa_cap - 1);
+  const int n_win = max(0, w_hi - w_lo + 1);
+  const int n_keys = n_sel + n_win;
+
+  // Q rows of this head group (zero rows past Hq)
+  for (int i = tid; i < kHG * (D / 8); i += kAttnThreads) {
+    const int h = i / (D / 8), c8 = i % (D / 8);
+    const int head = hg * kHG + h;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (head < a.Hq) v = *reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + head) * D + c8 * 8);
+    *reinterpret_cast<uint4*>(&sm.q[h * QS + c8 * 8]) = v;
+  }
+  if (tid < kHG) {
+    sm.m[tid] = -INFINITY;
+    sm.l[tid] = 0.f;
+  }
+
+  float o[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  const float sl2 = a.scale * 1.4426950408889634f;  // logits in log2 units
+
+  for (int k0 = 0; k0 < n_keys; k0 += kTK) {
+    // ---- key sources of this tile
+    if (tid < kTK) {
+      const int i = k0 + tid;
+      int64_t src = -1;
+      if (i < n_sel) {
+        const int j = a.idx[row * a.K + i];
+        if (j >= 0 && j < nv) src = entry_slot(a.page_table, a.max_pages, a.n_pages, b, j, status);
+        else raise_status(status, CSA2_STATUS_BAD_INDEX);
+      } else if (i < n_keys) {
+        src = -2 - (int64_t)(w_lo + (i - n_sel) - pos0);
+      }
+      sm.key_src[tid] = src;
+    }
+    __syncthreads();
+    // ---- gather + dequantise
+    for (int i = tid; i < kTK * (D / 16); i += kAttnThreads) {
+      const int kr = i / (D / 16), grp = i % (D / 16);
+      dequant_group<D>(a, b, sm.key_src[kr], grp, &sm.k[kr * QS + grp * 16]);
+    }
+    __syncthreads();
+    // ---- S = Q K^T : warp owns keys 16*warp .. +15
+    {
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t qa = smem_u32(&sm.q[(lane & 15) * QS + (lane >> 4) * 8]);
+      const int mi = lane >> 3, r8 = lane & 7;
+      const uint32_t kb = smem_u32(&sm.k[(warp * 16 + (mi >> 1) * 8 + r8) * QS + (mi & 1) * 8]);
+#pragma unroll 4
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+        ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
+        ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
+        mma16816(s0, a0, a1, a2, a3, b0, b1);
+        mma16816(s1, a0, a1, a2, a3, b2, b3);
+      }
+      const int key0 = warp * 16 + 2 * t4;
+      const bool v00 = sm.key_src[key0] != -1, v01 = sm.key_src[key0 + 1] != -1;
+      const bool v10 = sm.key_src[key0 + 8] != -1, v11 = sm.key_src[key0 + 9] != -1;
+      sm.s[g * kTK + key0] = v00 ? s0[0] * sl2 : -INFINITY;
+      sm.s[g * kTK + key0 + 1] = v01 ? s0[1] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0] = v00 ? s0[2] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0 + 1] = v01 ? s0[3] * sl2 : -INFINITY;
+      sm.s[g * kTK + key0 + 8] = v10 ? s1[0] * sl2 : -INFINITY;
+      sm.s[g * kTK + key0 + 9] = v11 ? s1[1] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0 + 8] = v10 ? s1[2] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0 + 9] = v11 ? s1[3] * sl2 : -INFINITY;
+    }
+    __syncthreads();
+    // ---- online softmax: 8 threads per head, 8 keys each
+    {
+      const int h = tid >> 3, part = tid & 7;
+      float sv[8];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        sv[i] = sm.s[h * kTK + part * 8 + i];
+        mx = fmaxf(mx, sv[i]);
+      }
+#pragma unroll
+      for (int o2 = 1; o2 < 8; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      const float m_old = sm.m[h];
+      const float m_new = fmaxf(m_old, mx);
+      float sum = 0.f;
+      uint32_t pw[4];
+#pragma unroll
+      for (int i = 0; i < 8; i += 2) {
+        const float p0 = m_new == -INFINITY ? 0.f : exp2f(sv[i] - m_new);
+        const float p1 = m_new == -INFINITY ? 0.f : exp2f(sv[i + 1] - m_new);
+        const uint32_t b0 = f32_to_bf16_bits(p0), b1 = f32_to_bf16_bits(p1);
+        sum += bf16_bits_to_f32(b0) + bf16_bits_to_f32(b1);  // normalise by what PV uses
+        pw[i >> 1] = b0 | (b1 << 16);
+      }
+      *reinterpret_cast<uint4*>(&sm.p[h * PS + part * 8]) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+#pragma unroll
+      for (int o2 = 1; o2 < 8; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+      __syncwarp();
+      if (part == 0) {
+        const float al = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+        sm.alpha[h] = al;
+        sm.l[h] = sm.l[h] * al + sum;
+        sm.m[h] = m_new;
+      }
+    }
+    __syncthreads();
+    // ---- O = O * alpha + P V : warp owns channels warp*(D/4) .. +D/4
+    {
+      const float al0 = sm.alpha[g], al1 = sm.alpha[g + 8];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1;
+      }
+      const uint32_t pa = smem_u32(&sm.p[(lane & 15) * PS + (lane >> 4) * 8]);
+      const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+      for (int kk = 0; kk < kTK / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(pa + kk * 32, a0, a1, a2, a3);
+        const uint32_t vb = smem_u32(&sm.k[(kk * 16 + (mi & 1) * 8 + r8) * QS + warp * (D / 4) + (mi >> 1) * 8]);
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + np * 32, b0, b1, b2, b3);
+          mma16816(o[2 * np], a0, a1, a2, a3, b0, b1);
+          mma16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- normalise and store
+  const float l0 = sm.l[g], l1 = sm.l[g + 8];
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int head0 = hg * kHG + g, head1 = head0 + 8;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const int ch = warp * (D / 4) + i * 8 + 2 * t4;
+    if (head0 < a.Hq)
+      *reinterpret_cast<float2*>(a.O + (row * a.Hq + head0) * D + ch) = make_float2(o[i][0] * inv0, o[i][1] * inv0);
+    if (head1 < a.Hq)
+      *reinterpret_cast<float2*>(a.O + (row * a.Hq + head1) * D + ch) = make_float2(o[i][2] * inv1, o[i][3] * inv1);
+  }
+  if (a.lse && tid < kHG && hg * kHG + tid < a.Hq) {
+    const float l = sm.l[tid];
+    a.lse[row * a.Hq + hg * kHG + tid] = l > 0.f ? (sm.m[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
+template <int D>
+static cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(AttnSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(k_sparse_attn<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((a.Hq + kHG - 1) / kHG, (unsigned)((int64_t)a.B * a.Tq));
+  k_sparse_attn<D><<<grid, kAttnThreads, smem, s>>>(a, status_word());
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s) {
+  if ((int64_t)a.B * a.Tq == 0) return cudaSuccess;
+  if (a.d == 512) return launch_attn_d<512>(a, s);
+  return launch_attn_d<64>(a, s);
+}
+
+}  // namespace csa2

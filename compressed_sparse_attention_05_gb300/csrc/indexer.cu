@@ -1,0 +1,319 @@
+// Sparse-indexer scoring: s_j = sum_h w_h * ReLU(q_h . k_j) for every
+// causally visible compressed entry (Full) or for the pooled positions only
+// (Reindex).  "DeepSeek-V4.1 架构解析" §02: the indexer scores every visible
+// entry and keeps a Top-512; Reindex layers rescore the shared indexer keys
+// with their own query, inside the 2,048 x 8 pool.  Score form: reading R6.
+//
+// Decode is bound by HBM: every visible key (Di bf16) is read exactly once.
+// The bf16 path runs on tensor cores (m16n8k16, fp32 accumulate), entries as
+// the M dimension and heads as N, so the ALU stays far below the 8 FLOP/B the
+// scan needs.  Each thread loads its A fragments straight from the paged key
+// rows with 16-byte loads: the head dimension is visited in a permuted order
+// (the same permutation for q and k, so the dot products are unchanged) that
+// makes every warp load instruction touch 16 full 32-byte sectors.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Visible positions (0..8) of pooled block `blk` when nv entries are visible.
+__device__ __forceinline__ int visible_in_block(int nv, int32_t blk) {
+  const int64_t v = (int64_t)nv - 8LL * blk;
+  return v <= 0 ? 0 : (v >= 8 ? 8 : (int)v);
+}
+
+constexpr int kIdxWarps = 8;          // warps per CTA
+constexpr int kIdxTilesPerWarp = 4;   // 16-entry tiles per warp
+constexpr int kIdxChunk = kIdxWarps * kIdxTilesPerWarp * 16;  // entries per CTA
+
+// Scores of one 16-entry tile for one query from A fragments already in
+// registers.  Returns (via out_g, out_g8) the scores of entries g and g+8.
+template <int NCH, int NT>
+__device__ __forceinline__ void tile_scores(const uint4 (&ka)[NCH], const uint4 (&kb)[NCH],
+                                            const uint4 (&qf)[NT][NCH], const float (&wv)[NT][2],
+                                            float& out_g, float& out_g8) {
+  float acc_g = 0.f, acc_g8 = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      mma_bf16_16816(d, ka[c].x, kb[c].x, ka[c].y, kb[c].y, qf[nt][c].x, qf[nt][c].y);
+      mma_bf16_16816(d, ka[c].z, kb[c].z, ka[c].w, kb[c].w, qf[nt][c].z, qf[nt][c].w);
+    }
+    acc_g += wv[nt][0] * fmaxf(d[0], 0.f) + wv[nt][1] * fmaxf(d[1], 0.f);
+    acc_g8 += wv[nt][0] * fmaxf(d[2], 0.f) + wv[nt][1] * fmaxf(d[3], 0.f);
+  }
+  acc_g += __shfl_xor_sync(0xffffffffu, acc_g, 1);
+  acc_g += __shfl_xor_sync(0xffffffffu, acc_g, 2);
+  acc_g8 += __shfl_xor_sync(0xffffffffu, acc_g8, 1);
+  acc_g8 += __shfl_xor_sync(0xffffffffu, acc_g8, 2);
+  out_g = acc_g;
+  out_g8 = acc_g8;
+}
+
+// Query fragments of head group nt for the thread (g, t): heads 8nt + g,
+// dims 32c + 8t .. +7 (zero for heads >= Hi).
+template <int NCH, int NT>
+__device__ __forceinline__ void load_query(const uint16_t* __restrict__ q, const float* __restrict__ w,
+                                           int Hi, int Di, int lane, uint4 (&qf)[NT][NCH],
+                                           float (&wv)[NT][2]) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int h = nt * 8 + g;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c)
+      qf[nt][c] = h < Hi ? *reinterpret_cast<const uint4*>(q + (int64_t)h * Di + 32 * c + 8 * t)
+                         : make_uint4(0, 0, 0, 0);
+    const int h0 = nt * 8 + 2 * t;
+    wv[nt][0] = h0 < Hi ? w[h0] : 0.f;
+    wv[nt][1] = h0 + 1 < Hi ? w[h0 + 1] : 0.f;
+  }
+}
+
+// Full mode.  grid = (entry chunks, query groups, B); a CTA scores one chunk
+// of kIdxChunk entries of sequence b against QG consecutive query tokens.
+template <int NCH, int NT>
+__global__ void __launch_bounds__(kIdxWarps * 32)
+k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t stride,
+                   float* __restrict__ blockmax, int64_t bm_stride, uint32_t* status) {
+  const int b = blockIdx.z;
+  const int i0 = blockIdx.y * QG;
+  const int i1 = min(a.Tq, i0 + QG);
+  const int n_ent = min(a.n_entries[b], a.max_entries);
+  int max_vis = 0;
+  for (int i = i0; i < i1; ++i) max_vis = max(max_vis, n_visible(n_ent, a.q_pos[(int64_t)b * a.Tq + i]));
+  const int chunk0 = blockIdx.x * kIdxChunk;
+  if (chunk0 >= max_vis) return;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const uint16_t* kbase = reinterpret_cast<const uint16_t*>(a.k);
+  for (int tt = 0; tt < kIdxTilesPerWarp; ++tt) {
+    const int e0 = chunk0 + (warp * kIdxTilesPerWarp + tt) * 16;
+    if (e0 >= max_vis) break;
+    const int64_t slot0 = entry_slot(a.page_table, a.max_pages, a.n_pages, b, e0, status);
+    if (slot0 < 0) continue;
+    uint4 ka[NCH], kb[NCH];
+    const uint16_t* rg = kbase + (slot0 + g) * a.Di + 8 * t;
+    const uint16_t* rg8 = kbase + (slot0 + g + 8) * a.Di + 8 * t;
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+      ka[c] = __ldg(reinterpret_cast<const uint4*>(rg + 32 * c));
+      kb[c] = __ldg(reinterpret_cast<const uint4*>(rg8 + 32 * c));
+    }
+    for (int i = i0; i < i1; ++i) {
+      const int64_t row = (int64_t)b * a.Tq + i;
+      const int nv = n_visible(n_ent, a.q_pos[row]);
+      if (e0 >= nv) continue;
+      uint4 qf[NT][NCH];
+      float wv[NT][2];
+      load_query<NCH, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi,
+                          a.Hi, a.Di, lane, qf, wv);
+      float sg, sg8;
+      tile_scores<NCH, NT>(ka, kb, qf, wv, sg, sg8);
+      const bool vg = e0 + g < nv, vg8 = e0 + g + 8 < nv;
+      if (t == 0 && vg) scores[row * stride + e0 + g] = sg;
+      if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
+      if (blockmax) {
+        float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+        }
+        if (lane == 0) blockmax[row * bm_stride + e0 / 8] = m0;
+        if (lane == 1 && e0 + 8 < nv) blockmax[row * bm_stride + e0 / 8 + 1] = m1;
+      }
+    }
+  }
+}
+
+// Reindex.  grid = (pool-block pairs / kIdxWarps, rows): warp w scores the
+// two pooled blocks 2p, 2p+1 (16 positions = one tile; rows g -> block 2p,
+// rows g+8 -> block 2p+1) into compact columns 8*slot + e.
+template <int NCH, int NT>
+__global__ void __launch_bounds__(kIdxWarps * 32)
+k_index_scores_pool_mma(IndexerArgs a, const int32_t* __restrict__ pool,
+                        const int32_t* __restrict__ pool_cnt, int n_pool,
+                        float* __restrict__ scores, int64_t stride, int32_t* __restrict__ n_valid,
+                        uint32_t* status) {
+  const int64_t row = blockIdx.y;
+  const int b = (int)(row / a.Tq);
+  const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[row]);
+  const int pc = min(max(pool_cnt[row], 0), n_pool);
+  const int32_t* prow = pool + row * n_pool;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  if (blockIdx.x == 0 && warp == 0) {
+    int cnt = 0;
+    for (int p = lane; p < pc; p += 32) cnt += visible_in_block(nv, prow[p]);
+    cnt = (int)warp_sum((float)cnt);
+    if (lane == 0) n_valid[row] = cnt;
+  }
+  const int pair = blockIdx.x * kIdxWarps + warp;
+  const int p0 = 2 * pair;
+  if (p0 >= pc) return;
+  const int64_t blk0 = prow[p0];
+  const int64_t blk1 = p0 + 1 < pc ? prow[p0 + 1] : -1;
+  const int64_t e_g = 8 * blk0 + g;
+  const int64_t e_g8 = blk1 >= 0 ? 8 * blk1 + g : -1;
+  const bool vg = blk0 >= 0 && e_g < nv;
+  const bool vg8 = e_g8 >= 0 && e_g8 < nv;
+  if ((blk0 < 0 || 8 * blk0 >= nv) && lane == 0) raise_status(status, CSA2_STATUS_BAD_INDEX);
+  const int64_t sg_slot = vg ? entry_slot(a.page_table, a.max_pages, a.n_pages, b, (int)e_g, status) : -1;
+  const int64_t sg8_slot = vg8 ? entry_slot(a.page_table, a.max_pages, a.n_pages, b, (int)e_g8, status) : -1;
+  const uint16_t* kbase = reinterpret_cast<const uint16_t*>(a.k);
+  uint4 ka[NCH], kb[NCH];
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    ka[c] = sg_slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(kbase + sg_slot * a.Di + 8 * t + 32 * c))
+                         : make_uint4(0, 0, 0, 0);
+    kb[c] = sg8_slot >= 0 ? __ldg(reinterpret_cast<const uint4*>(kbase + sg8_slot * a.Di + 8 * t + 32 * c))
+                          : make_uint4(0, 0, 0, 0);
+  }
+  uint4 qf[NT][NCH];
+  float wv[NT][2];
+  load_query<NCH, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi, a.Hi,
+                      a.Di, lane, qf, wv);
+  float s0, s1;
+  tile_scores<NCH, NT>(ka, kb, qf, wv, s0, s1);
+  if (t == 0 && vg) scores[row * stride + 8 * p0 + g] = s0;
+  if (t == 1 && vg8) scores[row * stride + 8 * (p0 + 1) + g] = s1;
+}
+
+// Generic path (fp32 keys, or shapes the tensor-core path does not take):
+// one thread per (query, entry), query staged in shared memory.
+template <typename T>
+__device__ __forceinline__ float load_as_f32(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float load_as_f32<float>(const float* p, int64_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float load_as_f32<uint16_t>(const uint16_t* p, int64_t i) {
+  return bf16_bits_to_f32(p[i]);
+}
+
+template <typename T>
+__global__ void k_index_scores_generic(IndexerArgs a, const int32_t* __restrict__ pool,
+                                       const int32_t* __restrict__ pool_cnt, int n_pool,
+                                       float* __restrict__ scores, int64_t stride,
+                                       int32_t* __restrict__ n_valid, uint32_t* status) {
+  extern __shared__ float sq[];  // [Hi][Di] then w[Hi]
+  const int64_t row = blockIdx.y;
+  const int b = (int)(row / a.Tq);
+  const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[row]);
+  const T* q = reinterpret_cast<const T*>(a.q) + row * a.Hi * a.Di;
+  for (int i = threadIdx.x; i < a.Hi * a.Di; i += blockDim.x) sq[i] = load_as_f32<T>(q, i);
+  for (int i = threadIdx.x; i < a.Hi; i += blockDim.x) sq[a.Hi * a.Di + i] = a.w[row * a.Hi + i];
+  __syncthreads();
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int e;
+  if (pool) {
+    const int pc = min(max(pool_cnt[row], 0), n_pool);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      int cnt = 0;
+      for (int p = 0; p < pc; ++p) cnt += visible_in_block(nv, pool[row * n_pool + p]);
+      n_valid[row] = cnt;
+    }
+    if (c >= 8 * (int64_t)pc) return;
+    const int64_t ee = 8LL * pool[row * n_pool + c / 8] + (c % 8);
+    e = (ee < 0 || ee >= nv) ? -1 : (int)ee;
+  } else {
+    e = (int)c;
+  }
+  if (e < 0 || e >= nv || c >= stride) return;
+  const int64_t slot = entry_slot(a.page_table, a.max_pages, a.n_pages, b, e, status);
+  if (slot < 0) return;
+  const T* k = reinterpret_cast<const T*>(a.k) + slot * a.Di;
+  float s = 0.f;
+  for (int h = 0; h < a.Hi; ++h) {
+    float dot = 0.f;
+    for (int i = 0; i < a.Di; ++i) dot = fmaf(sq[h * a.Di + i], load_as_f32<T>(k, i), dot);
+    s += sq[a.Hi * a.Di + h] * fmaxf(dot, 0.f);
+  }
+  scores[row * stride + c] = s;
+}
+
+static bool mma_path(const IndexerArgs& a) {
+  return a.dtype == CSA2_BF16 && (a.Di == 32 || a.Di == 64 || a.Di == 128) && a.Hi <= 16;
+}
+
+template <int NCH, int NT>
+static cudaError_t launch_full_mma(const IndexerArgs& a, float* scores, int64_t stride,
+                                   float* blockmax, int64_t bm_stride, int max_entries,
+                                   cudaStream_t s) {
+  const int QG = a.Tq >= 16 ? 16 : a.Tq;
+  dim3 grid((max_entries + kIdxChunk - 1) / kIdxChunk, (a.Tq + QG - 1) / QG, a.B);
+  k_index_scores_mma<NCH, NT><<<grid, kIdxWarps * 32, 0, s>>>(a, QG, scores, stride, blockmax,
+                                                              bm_stride, status_word());
+  return counted(cudaGetLastError());
+}
+
+template <int NCH, int NT>
+static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, const int32_t* pool_cnt,
+                                   int n_pool, float* scores, int64_t stride, int32_t* n_valid,
+                                   cudaStream_t s) {
+  const int pairs = (n_pool + 1) / 2;
+  dim3 grid((pairs + kIdxWarps - 1) / kIdxWarps, a.B * a.Tq);
+  k_index_scores_pool_mma<NCH, NT><<<grid, kIdxWarps * 32, 0, s>>>(a, pool, pool_cnt, n_pool, scores,
+                                                                   stride, n_valid, status_word());
+  return counted(cudaGetLastError());
+}
+
+#define CSA2_DISPATCH_MMA(FN, ...)                                  \
+  do {                                                              \
+    const int nt = a.Hi > 8 ? 2 : 1;                                \
+    if (a.Di == 128) return nt == 1 ? FN<4, 1>(__VA_ARGS__) : FN<4, 2>(__VA_ARGS__); \
+    if (a.Di == 64) return nt == 1 ? FN<2, 1>(__VA_ARGS__) : FN<2, 2>(__VA_ARGS__);  \
+    return nt == 1 ? FN<1, 1>(__VA_ARGS__) : FN<1, 2>(__VA_ARGS__);                  \
+  } while (0)
+
+cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
+                                int64_t bm_stride, int block, int max_entries, cudaStream_t s) {
+  if ((int64_t)a.B * a.Tq == 0 || max_entries == 0) return cudaSuccess;
+  if (mma_path(a) && block == 8) {
+    CSA2_DISPATCH_MMA(launch_full_mma, a, scores, stride, blockmax, bm_stride, max_entries, s);
+  }
+  dim3 grid((max_entries + 255) / 256, a.B * a.Tq);
+  const size_t smem = (size_t)(a.Hi * a.Di + a.Hi) * sizeof(float);
+  if (a.dtype == CSA2_BF16)
+    k_index_scores_generic<uint16_t><<<grid, 256, smem, s>>>(a, nullptr, nullptr, 0, scores, stride,
+                                                              nullptr, status_word());
+  else
+    k_index_scores_generic<float><<<grid, 256, smem, s>>>(a, nullptr, nullptr, 0, scores, stride,
+                                                           nullptr, status_word());
+  cudaError_t e = counted(cudaGetLastError());
+  if (e != cudaSuccess || !blockmax) return e;
+  ValidSpec v{nullptr, a.n_entries, a.q_pos, a.Tq, 1, a.max_entries};
+  return launch_block_max(scores, (int64_t)a.B * a.Tq, stride, v, block, blockmax, bm_stride, s);
+}
+
+cudaError_t launch_index_scores_pool(const IndexerArgs& a, const int32_t* pool, const int32_t* pool_cnt,
+                                     int n_pool, int block, float* scores, int64_t stride,
+                                     int32_t* n_valid, cudaStream_t s) {
+  if ((int64_t)a.B * a.Tq == 0) return cudaSuccess;
+  if (mma_path(a) && block == 8) {
+    CSA2_DISPATCH_MMA(launch_pool_mma, a, pool, pool_cnt, n_pool, scores, stride, n_valid, s);
+  }
+  dim3 grid((unsigned)((8 * (int64_t)n_pool + 255) / 256), a.B * a.Tq);
+  const size_t smem = (size_t)(a.Hi * a.Di + a.Hi) * sizeof(float);
+  if (a.dtype == CSA2_BF16)
+    k_index_scores_generic<uint16_t><<<grid, 256, smem, s>>>(a, pool, pool_cnt, n_pool, scores,
+                                                              stride, n_valid, status_word());
+  else
+    k_index_scores_generic<float><<<grid, 256, smem, s>>>(a, pool, pool_cnt, n_pool, scores, stride,
+                                                           n_valid, status_word());
+  return counted(cudaGetLastError());
+}
+
+}  // namespace csa2

@@ -1,0 +1,127 @@
+// Launchers shared between the kernel translation units and the C-ABI layer
+// (api.cu).  Arguments are validated by the caller; launchers only launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// Device status word of the current device (see csa2_get_status).
+uint32_t* status_word();
+
+// Counts one kernel launch (csa2_launch_count) and returns the launch status.
+cudaError_t counted(cudaError_t launch_status);
+
+// ---- pack.cu ----------------------------------------------------------------
+cudaError_t launch_pack_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* codes,
+                              uint8_t* scales, cudaStream_t s);
+cudaError_t launch_unpack_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n_rows,
+                                int d, uint16_t* out, cudaStream_t s);
+cudaError_t launch_pack_fp8(const float* x, int64_t n_rows, int d, uint8_t* codes,
+                            float* scales, cudaStream_t s);
+// Window rows of query tokens: row (b, i) of x [B][Tq][d] goes to window row
+// q_pos[b][i] - pos0[b] of sequence b.
+cudaError_t launch_pack_fp8_window(const float* x, int B, int Tq, int d, const int32_t* q_pos,
+                                   const int32_t* pos0, int swa_cap, uint8_t* codes,
+                                   float* scales, cudaStream_t s);
+
+// Row source of the norm/rope/pack epilogue: either a plain fp32 latent
+// [B][n_max][d] or n_split fp32 partial sums [n_split][M][ld] (compression).
+struct LatentSource {
+  const float* base;
+  int64_t row_stride;    // elements between consecutive rows
+  int64_t split_stride;  // elements between split-K partials (0: one split)
+  int n_split;
+};
+cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r,
+                                  const float* gamma, float eps, float rope_base,
+                                  const int32_t* first_entry, const int32_t* n_rows,
+                                  const int32_t* page_table, int max_pages, int64_t n_pages,
+                                  uint8_t* kv_codes, uint8_t* kv_scales,
+                                  // optional indexer-key epilogue (compression)
+                                  const float* idx_src, int64_t idx_row_stride, int Di,
+                                  int idx_dtype, void* idx_k, cudaStream_t s);
+
+// ---- compress.cu --------------------------------------------------------------
+// C[split][m][n] = sum over the split's K-range of A[m][:] * Bw[n][:], where
+// A rows are the 4-token groups of hidden and Bw = [W; W_idx] (n < d: W).
+size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out);
+cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H,
+                                 const uint16_t* W, int d, const uint16_t* W_idx, int Di,
+                                 float* partials, int n_split, cudaStream_t s);
+
+// ---- indexer.cu ---------------------------------------------------------------
+struct IndexerArgs {
+  const void* q;      // [rows][Hi][Di]
+  const float* w;     // [rows][Hi]
+  const void* k;      // [n_pages][64][Di]
+  const int32_t* page_table;
+  const int32_t* n_entries;  // [B]
+  const int32_t* q_pos;      // [rows]
+  int B, Tq, Hi, Di, dtype, max_pages;
+  int64_t n_pages;
+  int max_entries;           // visible counts are clamped to this (buffer bound)
+};
+// Full: scores[row][j] for visible j; blockmax (nullable) per `block` entries.
+cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride,
+                                float* blockmax, int64_t bm_stride, int block, int max_entries,
+                                cudaStream_t s);
+// Reindex: compact scores[row][p*block + e] of the pooled blocks' visible
+// positions; n_valid[row] receives the compact count.
+cudaError_t launch_index_scores_pool(const IndexerArgs& a, const int32_t* pool,
+                                     const int32_t* pool_cnt, int n_pool, int block,
+                                     float* scores, int64_t stride, int32_t* n_valid,
+                                     cudaStream_t s);
+
+// ---- topk.cu --------------------------------------------------------------------
+// Number of valid columns of a row: n_valid[row] if given, else derived from
+// (n_entries[row / Tq], q_pos[row]) and divided (rounding up) by `divisor`,
+// else `stride`.
+struct ValidSpec {
+  const int32_t* n_valid;
+  const int32_t* n_entries;
+  const int32_t* q_pos;
+  int Tq;
+  int divisor;
+  int64_t max_n;   // > 0: entry counts derived from n_entries are clamped to it first
+};
+// Optional index remap for Reindex: out = pool[row][c / block] * block + c % block.
+struct Remap {
+  const int32_t* pool;
+  int64_t pool_stride;
+  int block;
+};
+cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
+                        int32_t* out_idx, int32_t* out_cnt, Remap remap, cudaStream_t s);
+// Block maxima of the valid columns: out[row][b] = max(scores[row][block*b ..]).
+cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, ValidSpec v,
+                             int block, float* out, int64_t out_stride, cudaStream_t s);
+
+// ---- attention.cu -------------------------------------------------------------
+struct AttnArgs {
+  const uint16_t* Q;          // [rows][Hq][d] bf16
+  const uint8_t* kv_codes;
+  const uint8_t* kv_scales;
+  const int32_t* page_table;
+  int64_t n_pages;
+  int max_pages;
+  const int32_t* idx;         // [rows][K]
+  const int32_t* cnt;         // [rows]
+  const int32_t* q_pos;       // [rows]
+  const int32_t* n_entries;   // [B]
+  const uint8_t* swa_codes;   // [B][swa_cap][d]
+  const float* swa_scales;    // [B][swa_cap]
+  const int32_t* swa_pos0;    // [B]
+  int swa_cap, W;
+  int B, Tq, Hq, d, K;
+  float scale;
+  float* O;                   // [rows][Hq][d]
+  float* lse;                 // [rows][Hq] or null
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s);
+
+}  // namespace csa2

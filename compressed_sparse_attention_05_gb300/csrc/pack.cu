@@ -1,0 +1,243 @@
+// Packing kernels: MXFP4 main KV (with RMSNorm + RoPE in front), FP8 window.
+//
+// Formats follow "DeepSeek-V4.1 架构解析" §03: E2M1 values with one E4M3 scale
+// per 16 channels and no global scale, quantised after RoPE; the sliding
+// window stays FP8.  Rounding rules: readings R2-R5 of include/csa2.h.
+// Bandwidth-bound: every kernel reads and writes each byte once with 16-byte
+// (or 8-byte) accesses.  Built without fast-math: the divisions that decide a
+// code are IEEE fp32 divisions, as the bit-exact contract requires.
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+// One thread per 16-channel group of a contiguous fp32 array.
+__global__ void k_pack_mxfp4(const float* __restrict__ x, int64_t n_groups,
+                             uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const float4* src = reinterpret_cast<const float4*>(x + g * 16);
+  float v[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float4 f = src[i];
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+  Mxfp4Group p = pack_group16(v);
+  reinterpret_cast<uint2*>(codes)[g] = p.codes;
+  scales[g] = (uint8_t)p.scale;
+}
+
+__global__ void k_unpack_mxfp4(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                               int64_t n_groups, uint16_t* __restrict__ out) {
+  const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= n_groups) return;
+  const uint2 c = reinterpret_cast<const uint2*>(codes)[g];
+  const float s = e4m3_to_f32(scales[g]);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t word = i < 4 ? c.x : c.y;
+    const int sh = (i & 3) * 8;
+    const uint32_t lo = (word >> sh) & 0xFu, hi = (word >> (sh + 4)) & 0xFu;
+    // e2m1 * e4m3 has at most 6 significant bits: the product is exact and
+    // its bf16 pattern is the top half of the fp32 pattern
+    const float a = bf16_bits_to_f32(e2m1_to_bf16_bits(lo)) * s;
+    const float b = bf16_bits_to_f32(e2m1_to_bf16_bits(hi)) * s;
+    w[i] = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + g * 16);
+  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// One warp per row of d channels: scale = amax / 448, codes = E4M3(x / scale).
+__device__ __forceinline__ void fp8_row(const float* __restrict__ x, int d, uint8_t* __restrict__ codes,
+                                        float* scale_out, int lane) {
+  float amax = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 f = *reinterpret_cast<const float4*>(x + c);
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+  }
+  amax = warp_max(amax);
+  const float s = amax / 448.0f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 f = *reinterpret_cast<const float4*>(x + c);
+    uint32_t w = 0;
+    if (s != 0.f) {
+      w = f32_to_e4m3(f.x / s) | (f32_to_e4m3(f.y / s) << 8) | (f32_to_e4m3(f.z / s) << 16) |
+          (f32_to_e4m3(f.w / s) << 24);
+    }
+    *reinterpret_cast<uint32_t*>(codes + c) = w;
+  }
+  if (lane == 0) *scale_out = s;
+}
+
+__global__ void k_pack_fp8(const float* __restrict__ x, int64_t n_rows, int d,
+                           uint8_t* __restrict__ codes, float* __restrict__ scales) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= n_rows) return;
+  fp8_row(x + row * d, d, codes + row * d, scales + row, threadIdx.x & 31);
+}
+
+__global__ void k_pack_fp8_window(const float* __restrict__ x, int B, int Tq, int d,
+                                  const int32_t* __restrict__ q_pos, const int32_t* __restrict__ pos0,
+                                  int swa_cap, uint8_t* __restrict__ codes,
+                                  float* __restrict__ scales, uint32_t* status) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
+  if (row >= (int64_t)B * Tq) return;
+  const int b = (int)(row / Tq);
+  const int64_t wr = (int64_t)q_pos[row] - pos0[b];
+  if (wr < 0 || wr >= swa_cap) {
+    if ((threadIdx.x & 31) == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    return;
+  }
+  const int64_t dst = (int64_t)b * swa_cap + wr;
+  fp8_row(x + row * d, d, codes + dst * d, scales + dst, threadIdx.x & 31);
+}
+
+// RMSNorm + RoPE + MXFP4 pack + paged store of one entry per warp.  Lane l
+// owns channels 16l .. 16l+15 (one MXFP4 group); d <= 512.
+constexpr int kNrpWarps = 4;
+
+__global__ void __launch_bounds__(kNrpWarps * 32)
+k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
+                 float eps, float rope_base, const int32_t* __restrict__ first_entry,
+                 const int32_t* __restrict__ n_rows, const int32_t* __restrict__ page_table,
+                 int max_pages, int64_t n_pages, uint8_t* __restrict__ kv_codes,
+                 uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
+                 int Di, int idx_dtype, void* idx_k, uint32_t* status) {
+  __shared__ float row_buf[kNrpWarps][512];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
+  if (m >= (int64_t)B * n_max) return;
+  const int b = (int)(m / n_max), i = (int)(m % n_max);
+  if (n_rows && i >= n_rows[b]) return;
+  const int e = first_entry[b] + i;
+  const int64_t slot = entry_slot(page_table, max_pages, n_pages, b, e, status);
+  if (slot < 0) return;
+
+  const int n_groups = d / 16;
+  const bool has = lane < n_groups;
+  float v[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = 0.f;
+  if (has) {
+    for (int sp = 0; sp < src.n_split; ++sp) {   // fixed order: deterministic
+      const float4* p = reinterpret_cast<const float4*>(src.base + sp * src.split_stride +
+                                                        m * src.row_stride + lane * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 f = p[q];
+        v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
+      }
+    }
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) ss += v[c] * v[c];
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  if (has) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      v[c] = v[c] * inv * gamma[lane * 16 + c];
+      row_buf[warp][lane * 16 + c] = v[c];
+    }
+  }
+  __syncwarp();
+  // rotate-half RoPE on channels [d - r, d) at position 4e + 3
+  const int half = r / 2;
+  const double pos = 4.0 * (double)e + 3.0;
+  if (has && r > 0) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int ch = lane * 16 + c;
+      if (ch < d - r) continue;
+      const bool first = ch < d - half;
+      const int pi = first ? ch - (d - r) : ch - (d - half);
+      const double inv_freq = pow((double)rope_base, -2.0 * (double)pi / (double)r);
+      double sn, cs;
+      sincos(pos * inv_freq, &sn, &cs);
+      const double self = (double)row_buf[warp][ch];
+      if (first) {
+        const double other = (double)row_buf[warp][ch + half];
+        v[c] = (float)(self * cs - other * sn);
+      } else {
+        const double other = (double)row_buf[warp][ch - half];
+        v[c] = (float)(other * sn + self * cs);
+      }
+    }
+  }
+  if (has) {
+    Mxfp4Group g = pack_group16(v);
+    reinterpret_cast<uint2*>(kv_codes + slot * (d / 2))[lane] = g.codes;
+    kv_scales[slot * (d / 16) + lane] = (uint8_t)g.scale;
+  }
+  // indexer key of the entry (compression epilogue): sum the split partials
+  if (idx_k) {
+    for (int c = lane; c < Di; c += 32) {
+      float acc = 0.f;
+      for (int sp = 0; sp < src.n_split; ++sp)
+        acc += idx_src[sp * src.split_stride + m * idx_row_stride + c];
+      if (idx_dtype == CSA2_BF16)
+        reinterpret_cast<uint16_t*>(idx_k)[slot * Di + c] = (uint16_t)f32_to_bf16_bits(acc);
+      else
+        reinterpret_cast<float*>(idx_k)[slot * Di + c] = acc;
+    }
+  }
+}
+
+static inline unsigned grid_for(int64_t n, int per_block) {
+  return (unsigned)((n + per_block - 1) / per_block);
+}
+
+cudaError_t launch_pack_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* codes,
+                              uint8_t* scales, cudaStream_t s) {
+  const int64_t n = n_rows * (d / 16);
+  if (n == 0) return cudaSuccess;
+  k_pack_mxfp4<<<grid_for(n, 256), 256, 0, s>>>(x, n, codes, scales);
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_unpack_mxfp4(const uint8_t* codes, const uint8_t* scales, int64_t n_rows,
+                                int d, uint16_t* out, cudaStream_t s) {
+  const int64_t n = n_rows * (d / 16);
+  if (n == 0) return cudaSuccess;
+  k_unpack_mxfp4<<<grid_for(n, 256), 256, 0, s>>>(codes, scales, n, out);
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_pack_fp8(const float* x, int64_t n_rows, int d, uint8_t* codes,
+                            float* scales, cudaStream_t s) {
+  if (n_rows == 0) return cudaSuccess;
+  k_pack_fp8<<<grid_for(n_rows, 8), 256, 0, s>>>(x, n_rows, d, codes, scales);
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_pack_fp8_window(const float* x, int B, int Tq, int d, const int32_t* q_pos,
+                                   const int32_t* pos0, int swa_cap, uint8_t* codes,
+                                   float* scales, cudaStream_t s) {
+  const int64_t rows = (int64_t)B * Tq;
+  if (rows == 0) return cudaSuccess;
+  k_pack_fp8_window<<<grid_for(rows, 8), 256, 0, s>>>(x, B, Tq, d, q_pos, pos0, swa_cap, codes,
+                                                      scales, status_word());
+  return counted(cudaGetLastError());
+}
+
+cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r,
+                                  const float* gamma, float eps, float rope_base,
+                                  const int32_t* first_entry, const int32_t* n_rows,
+                                  const int32_t* page_table, int max_pages, int64_t n_pages,
+                                  uint8_t* kv_codes, uint8_t* kv_scales, const float* idx_src,
+                                  int64_t idx_row_stride, int Di, int idx_dtype, void* idx_k,
+                                  cudaStream_t s) {
+  const int64_t rows = (int64_t)B * n_max;
+  if (rows == 0) return cudaSuccess;
+  k_norm_rope_pack<<<grid_for(rows, kNrpWarps), kNrpWarps * 32, 0, s>>>(
+      src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
+      n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, status_word());
+  return counted(cudaGetLastError());
+}
+
+}  // namespace csa2
