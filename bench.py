@@ -68,6 +68,21 @@ def algorithmic(wl):
             "compress_flops": compress_flops}
 
 
+def replica_seed(seed: int, rank: int) -> int:
+    """Every rank runs an independent replica: its own seeded batch of sequences."""
+    return seed + 1000 * rank
+
+
+def max_over_ranks(x: float, dist, device="cpu") -> float:
+    """The slowest rank's value (the job is done when the last replica is)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t)
+
+
 def make_workload(name):
     from csa2_inputs import workloads as WL
     return WL.ALL[name]()
@@ -160,7 +175,7 @@ def run_gpu(args, rank, world, dist):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = make_workload(args.workload)
-    wl.seed += 1000 * rank                       # an independent replica per rank
+    wl.seed = replica_seed(wl.seed, rank)
     alg = algorithmic(wl)
     g = harness.LayerGroup(wl, f"cuda:{local}")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -191,11 +206,7 @@ def run_gpu(args, rank, world, dist):
     launches = abi.csa2_launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = sum(step_ms) / args.steps
-    ms_all = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_all = float(t)
+    ms_all = max_over_ranks(ms, dist, dev)
 
     # ---- dominant kernel, timed alone on the same stream through its own entry point
     kern = time_dominant_kernel(args, g, wl, flush, stream)
@@ -288,12 +299,8 @@ def time_e2e(args, g, flush, stream, dist):
         b.record(stream)
         b.synchronize()
         tot += a.elapsed_time(b)
-    ms = tot / n
+    ms = max_over_ranks(tot / n, dist, flush.device)
     world = dist.get_world_size() if dist is not None else 1
-    if dist is not None:
-        t = torch.tensor([ms], device=flush.device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t)
     wl = g.wl
     return {"value": world * wl.B * wl.Tq / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}

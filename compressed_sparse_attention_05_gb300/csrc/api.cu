@@ -64,6 +64,13 @@ static size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
     if (!(p)) return fail(CSA2_ERR_INVALID_ARG, "%s must not be NULL", #p);         \
     if (!aligned16(p)) return fail(CSA2_ERR_INVALID_ARG, "%s must be 16-byte aligned", #p); \
   } while (0)
+// int32 index / count / position arrays are read element-wise: 4-byte alignment
+#define REQUIRE_IPTR(p)                                                             \
+  do {                                                                              \
+    if (!(p)) return fail(CSA2_ERR_INVALID_ARG, "%s must not be NULL", #p);         \
+    if (reinterpret_cast<uintptr_t>(p) & 3u)                                        \
+      return fail(CSA2_ERR_INVALID_ARG, "%s must be 4-byte aligned", #p);           \
+  } while (0)
 #define LAUNCH(expr, what)                          \
   do {                                              \
     cudaError_t e_ = (expr);                        \
@@ -92,8 +99,8 @@ static int check_dims(const csa2_dims* dm, bool need_indexer, bool need_attn) {
 
 static int check_cache(const csa2_cache* c, bool need_kv, bool need_idx) {
   REQUIRE(c, "cache must not be NULL");
-  REQUIRE_PTR(c->page_table);
-  REQUIRE_PTR(c->n_entries);
+  REQUIRE_IPTR(c->page_table);
+  REQUIRE_IPTR(c->n_entries);
   REQUIRE(c->n_pages >= 1, "cache.n_pages must be >= 1");
   if (need_kv) {
     REQUIRE_PTR(c->kv_codes);
@@ -114,8 +121,10 @@ static IndexerArgs indexer_args(const csa2_dims* dm, const csa2_cache* c, const 
 }
 
 // Workspace of csa2_index_topk: scores, block maxima, valid counts.
+constexpr int kHistBins = 2048;  // score-key histogram bins per row (top 11 key bits)
+
 struct IndexWs {
-  size_t scores_off, bm_off, nvalid_off, total;
+  size_t scores_off, bm_off, nvalid_off, hist_off, total;
   int64_t s_stride, bm_stride;
 };
 static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
@@ -130,7 +139,8 @@ static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
   L.scores_off = 0;
   L.bm_off = round_up(L.scores_off + (size_t)(rows * L.s_stride) * 4, 256);
   L.nvalid_off = round_up(L.bm_off + (size_t)(rows * L.bm_stride) * 4, 256);
-  L.total = round_up(L.nvalid_off + (size_t)rows * 4, 256);
+  L.hist_off = round_up(L.nvalid_off + (size_t)rows * 4, 256);
+  L.total = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
   return L;
 }
 
@@ -202,8 +212,8 @@ int csa2_norm_rope_pack(const float* latent, int32_t B, int32_t n_max, int32_t d
   REQUIRE(r >= 0 && r <= d && r % 2 == 0, "r must be even and in 0..d (got %d)", r);
   REQUIRE(eps >= 0.f, "eps must be >= 0");
   if ((int64_t)B * n_max == 0) return CSA2_OK;
-  REQUIRE_PTR(latent); REQUIRE_PTR(gamma); REQUIRE_PTR(first_entry); REQUIRE_PTR(n_rows);
-  REQUIRE_PTR(page_table); REQUIRE_PTR(kv_codes); REQUIRE_PTR(kv_scales);
+  REQUIRE_PTR(latent); REQUIRE_PTR(gamma); REQUIRE_IPTR(first_entry); REQUIRE_IPTR(n_rows);
+  REQUIRE_IPTR(page_table); REQUIRE_PTR(kv_codes); REQUIRE_PTR(kv_scales);
   REQUIRE(max_pages >= 1 && n_pages >= 1, "max_pages and n_pages must be >= 1");
   LatentSource src{latent, d, 0, 1};
   LAUNCH(launch_norm_rope_pack(src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table,
@@ -231,7 +241,7 @@ int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, 
   REQUIRE(H % 64 == 0, "H must be a multiple of 64 (got %d)", H);
   REQUIRE(dm->r >= 0 && dm->r <= dm->d && dm->r % 2 == 0, "r must be even and in 0..d");
   if (B == 0 || T < 4) return CSA2_OK;
-  REQUIRE_PTR(hidden); REQUIRE_PTR(W); REQUIRE_PTR(gamma); REQUIRE_PTR(first_entry);
+  REQUIRE_PTR(hidden); REQUIRE_PTR(W); REQUIRE_PTR(gamma); REQUIRE_IPTR(first_entry);
   rc = check_cache(c, true, W_idx != nullptr);
   if (rc) return rc;
   if (W_idx) {
@@ -265,7 +275,7 @@ int csa2_index_scores(const csa2_dims* dm, const csa2_cache* c, const void* idx_
   if ((int64_t)dm->B * dm->Tq == 0) return CSA2_OK;
   rc = check_cache(c, false, true);
   if (rc) return rc;
-  REQUIRE_PTR(idx_q); REQUIRE_PTR(w); REQUIRE_PTR(q_pos); REQUIRE_PTR(scores);
+  REQUIRE_PTR(idx_q); REQUIRE_PTR(w); REQUIRE_IPTR(q_pos); REQUIRE_PTR(scores);
   REQUIRE(score_stride >= 1 && score_stride < (1LL << 31), "score_stride out of range");
   if (blockmax) {
     REQUIRE(dm->pool_block == 8, "pool_block must be 8");
@@ -273,7 +283,7 @@ int csa2_index_scores(const csa2_dims* dm, const csa2_cache* c, const void* idx_
   }
   IndexerArgs a = indexer_args(dm, c, idx_q, w, q_pos);
   a.max_entries = (int)score_stride;
-  LAUNCH(launch_index_scores(a, scores, score_stride, blockmax, bm_stride, 8, (int)score_stride,
+  LAUNCH(launch_index_scores(a, scores, score_stride, blockmax, bm_stride, 8, (int)score_stride, nullptr,
                              static_cast<cudaStream_t>(stream)),
          "index_scores");
   return CSA2_OK;
@@ -292,10 +302,10 @@ int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32
   REQUIRE(stride >= 1 && stride < (1LL << 31), "stride out of range");
   REQUIRE(k >= 1 && k <= 4096, "k must be in 1..4096 (got %d)", k);
   if (rows == 0) return CSA2_OK;
-  REQUIRE_PTR(scores); REQUIRE_PTR(out_idx); REQUIRE_PTR(out_cnt);
-  if (n_valid) REQUIRE(aligned16(n_valid), "n_valid must be 16-byte aligned");
+  REQUIRE_PTR(scores); REQUIRE_IPTR(out_idx); REQUIRE_IPTR(out_cnt);
+  if (n_valid) REQUIRE_IPTR(n_valid);
   ValidSpec v{n_valid, nullptr, nullptr, 1, 1, 0};
-  LAUNCH(launch_topk(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8},
+  LAUNCH(launch_topk(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, nullptr, 0,
                      static_cast<cudaStream_t>(stream)),
          "topk");
   return CSA2_OK;
@@ -310,7 +320,7 @@ int csa2_block_pool_f32(const float* scores, int64_t rows, int64_t stride, const
   REQUIRE(block >= 1 && block <= 64, "block must be in 1..64");
   REQUIRE(n_pool_blocks >= 1 && n_pool_blocks <= 4096, "n_pool_blocks must be in 1..4096");
   if (rows == 0) return CSA2_OK;
-  REQUIRE_PTR(scores); REQUIRE_PTR(n_valid); REQUIRE_PTR(out_pool); REQUIRE_PTR(out_pool_cnt);
+  REQUIRE_PTR(scores); REQUIRE_IPTR(n_valid); REQUIRE_IPTR(out_pool); REQUIRE_IPTR(out_pool_cnt);
   const int64_t nb = (stride + block - 1) / block;
   float* bm = out_blockmax;
   int64_t bm_stride = nb;
@@ -326,7 +336,8 @@ int csa2_block_pool_f32(const float* scores, int64_t rows, int64_t stride, const
   LAUNCH(launch_block_max(scores, rows, stride, ve, block, bm, bm_stride, s), "block_max");
   // valid blocks per row: ceil(n_valid / block)
   ValidSpec vd{n_valid, nullptr, nullptr, 1, block, 0};
-  LAUNCH(launch_topk(bm, rows, bm_stride, vd, n_pool_blocks, out_pool, out_pool_cnt, Remap{nullptr, 0, 8}, s),
+  LAUNCH(launch_topk(bm, rows, bm_stride, vd, n_pool_blocks, out_pool, out_pool_cnt, Remap{nullptr, 0, 8},
+                     nullptr, 0, s),
          "block_pool_topk");
   return CSA2_OK;
 }
@@ -346,15 +357,15 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   if (rows == 0) return CSA2_OK;
   rc = check_cache(c, false, true);
   if (rc) return rc;
-  REQUIRE_PTR(idx_q); REQUIRE_PTR(w); REQUIRE_PTR(q_pos); REQUIRE_PTR(out_idx); REQUIRE_PTR(out_cnt);
+  REQUIRE_PTR(idx_q); REQUIRE_PTR(w); REQUIRE_IPTR(q_pos); REQUIRE_IPTR(out_idx); REQUIRE_IPTR(out_cnt);
   REQUIRE(max_entries >= 0, "max_entries must be >= 0");
   const bool reindex = pool != nullptr;
   if (reindex || out_pool) {
     REQUIRE(dm->pool_block == 8, "pool_block must be 8 (got %d)", dm->pool_block);
     REQUIRE(dm->n_pool_blocks >= 1 && dm->n_pool_blocks <= 4096, "n_pool_blocks must be in 1..4096");
   }
-  if (reindex) { REQUIRE_PTR(pool); REQUIRE_PTR(pool_cnt); }
-  if (out_pool) { REQUIRE_PTR(out_pool); REQUIRE_PTR(out_pool_cnt); }
+  if (reindex) { REQUIRE_IPTR(pool); REQUIRE_IPTR(pool_cnt); }
+  if (out_pool) { REQUIRE_IPTR(out_pool); REQUIRE_IPTR(out_pool_cnt); }
   const IndexWs L = index_ws_layout(dm, max_entries);
   if (!ws || ws_bytes < L.total) return fail(CSA2_ERR_WORKSPACE, "index_topk needs %zu workspace bytes (got %zu)", L.total, ws_bytes);
   REQUIRE(aligned16(ws), "ws must be 16-byte aligned");
@@ -362,17 +373,20 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   float* scores = reinterpret_cast<float*>(base + L.scores_off);
   float* bm = reinterpret_cast<float*>(base + L.bm_off);
   int32_t* nvalid = reinterpret_cast<int32_t*>(base + L.nvalid_off);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(base + L.hist_off);
   IndexerArgs a = indexer_args(dm, c, idx_q, w, q_pos);
   a.max_entries = max_entries;
   if (!reindex) {
-    LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, s),
+    LAUNCH(cudaMemsetAsync(hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
+    LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s),
            "index_scores");
     ValidSpec v{nullptr, c->n_entries, q_pos, dm->Tq, 1, max_entries};
-    LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, s), "topk");
+    LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins, s),
+           "topk");
     if (out_pool) {
       ValidSpec vb{nullptr, c->n_entries, q_pos, dm->Tq, 8, max_entries};
       LAUNCH(launch_topk(bm, rows, L.bm_stride, vb, dm->n_pool_blocks, out_pool, out_pool_cnt,
-                         Remap{nullptr, 0, 8}, s),
+                         Remap{nullptr, 0, 8}, nullptr, 0, s),
              "block_pool");
     }
   } else {
@@ -380,7 +394,7 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
            "index_scores_pool");
     ValidSpec v{nvalid, nullptr, nullptr, 1, 1, 0};
     LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt,
-                       Remap{pool, dm->n_pool_blocks, 8}, s),
+                       Remap{pool, dm->n_pool_blocks, 8}, nullptr, 0, s),
            "reindex_topk");
   }
   return CSA2_OK;
@@ -404,10 +418,10 @@ static int attn_impl(const csa2_dims* dm, const csa2_cache* c, const csa2_window
   rc = check_cache(c, true, false);
   if (rc) return rc;
   REQUIRE(win, "window must not be NULL");
-  REQUIRE_PTR(Q); REQUIRE_PTR(q_pos); REQUIRE_PTR(idx); REQUIRE_PTR(cnt); REQUIRE_PTR(O);
+  REQUIRE_PTR(Q); REQUIRE_IPTR(q_pos); REQUIRE_IPTR(idx); REQUIRE_IPTR(cnt); REQUIRE_PTR(O);
   if (lse) REQUIRE(aligned16(lse), "lse must be 16-byte aligned");
   if (dm->swa_cap > 0 && dm->W > 0) {
-    REQUIRE_PTR(win->codes); REQUIRE_PTR(win->scales); REQUIRE_PTR(win->pos0);
+    REQUIRE_PTR(win->codes); REQUIRE_PTR(win->scales); REQUIRE_IPTR(win->pos0);
   }
   AttnArgs a;
   a.Q = Q; a.kv_codes = c->kv_codes; a.kv_scales = c->kv_scales; a.page_table = c->page_table;
@@ -448,10 +462,10 @@ int csa2_layer(const csa2_layer_args* a, void* ws, size_t ws_bytes, void* stream
   if (rc) return rc;
   const int64_t rows = (int64_t)dm->B * dm->Tq;
   if (rows == 0) return CSA2_OK;
-  REQUIRE_PTR(a->q_pos); REQUIRE_PTR(a->idx_out); REQUIRE_PTR(a->cnt_out);
-  if (a->mode == CSA2_MODE_REUSE) { REQUIRE_PTR(a->idx_in); REQUIRE_PTR(a->cnt_in); }
-  if (a->mode == CSA2_MODE_REINDEX) { REQUIRE_PTR(a->pool); REQUIRE_PTR(a->pool_cnt); }
-  if (a->mode == CSA2_MODE_FULL && a->hierarchical) { REQUIRE_PTR(a->pool); REQUIRE_PTR(a->pool_cnt); }
+  REQUIRE_IPTR(a->q_pos); REQUIRE_IPTR(a->idx_out); REQUIRE_IPTR(a->cnt_out);
+  if (a->mode == CSA2_MODE_REUSE) { REQUIRE_IPTR(a->idx_in); REQUIRE_IPTR(a->cnt_in); }
+  if (a->mode == CSA2_MODE_REINDEX) { REQUIRE_IPTR(a->pool); REQUIRE_IPTR(a->pool_cnt); }
+  if (a->mode == CSA2_MODE_FULL && a->hierarchical) { REQUIRE_IPTR(a->pool); REQUIRE_IPTR(a->pool_cnt); }
   const size_t need = csa2_layer_workspace_size(a);
   if (need && (!ws || ws_bytes < need)) return fail(CSA2_ERR_WORKSPACE, "layer needs %zu workspace bytes (got %zu)", need, ws_bytes);
   // 1. compression of the new tokens (Full only)
@@ -463,7 +477,7 @@ int csa2_layer(const csa2_layer_args* a, void* ws, size_t ws_bytes, void* stream
   // 2. window rows of the query tokens
   if (a->swa_new) {
     REQUIRE_PTR(a->swa_new); REQUIRE_PTR(a->window.codes); REQUIRE_PTR(a->window.scales);
-    REQUIRE_PTR(a->window.pos0);
+    REQUIRE_IPTR(a->window.pos0);
     LAUNCH(launch_pack_fp8_window(a->swa_new, dm->B, dm->Tq, dm->d, a->q_pos, a->window.pos0, dm->swa_cap,
                                   a->window.codes, a->window.scales, s),
            "pack_window");

@@ -4,18 +4,27 @@
 // kept in FP8, the last 128 raw tokens).  Head layout, key set and softmax:
 // reading R11 of include/csa2.h.
 //
-// One CTA per (query token, group of 16 heads), 4 warps.  Per 64-key tile:
-// gather + dequantise the keys into shared memory as bf16 (MXFP4 entries are
-// exact in bf16; window rows are bf16(e4m3 * scale)), S = Q K^T on tensor
-// cores (m16n8k16, each warp 16 keys), online softmax in fp32 (exp2 domain),
-// then O += P V with each warp owning a quarter of the value channels.
-// K = V: the same shared-memory tile feeds both products.
+// One CTA per (query token, group of 16 heads), 8 warps.  Per 64-key tile:
+// gather + dequantise the keys into shared memory, S = Q K^T on tensor cores
+// (m16n8k16, each warp 8 keys), online softmax in fp32 (exp2 domain), then
+// O += P V with each warp owning an eighth of the value channels.  K = V: the
+// same shared-memory tile feeds both products.
+//
+// Operands are fp16.  MXFP4 entries are converted by cvt.rn.f16x2.e2m1x2 and
+// scaled in f16x2: e2m1 * e4m3 has at most 6 significant bits and lies in
+// [2^-10, 2688], so the values are exactly the bf16 dequantised latent.  Q and
+// the window rows are first rounded to bf16 (the operands the method
+// specifies) and carried in fp16, which holds every bf16 value of magnitude
+// in [2^-14, 65504] exactly; P is rounded to fp16 (11 significant bits).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace csa2 {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 256;
+constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kTK = 64;       // keys per tile
 constexpr int kHG = 16;       // heads per CTA
 
@@ -34,13 +43,34 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E2M1 codes (one byte, even channel in the low nibble) -> f16x2, low half first.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+  return r;
+}
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+// An fp32 value holding a bf16 value -> fp16 bits (exact inside the fp16 range).
+__device__ __forceinline__ uint32_t f32_to_f16_bits(float f) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(f));
 }
 
 template <int D>
@@ -55,7 +85,7 @@ struct AttnSmem {
   float m[kHG], l[kHG], alpha[kHG];
 };
 
-// Dequantise one 16-channel group of a key into 16 bf16 in shared memory.
+// Dequantise one 16-channel group of a key into 16 fp16 values in shared memory.
 template <int D>
 __device__ __forceinline__ void dequant_group(const AttnArgs& a, int b, int64_t src, int grp,
                                               uint16_t* dst) {
@@ -63,13 +93,11 @@ __device__ __forceinline__ void dequant_group(const AttnArgs& a, int b, int64_t 
   if (src >= 0) {
     const uint2 c = *reinterpret_cast<const uint2*>(a.kv_codes + src * (D / 2) + grp * 8);
     const float sc = e4m3_to_f32(a.kv_scales[src * (D / 16) + grp]);
+    const uint32_t s2 = f32_to_f16_bits(sc) * 0x10001u;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t word = i < 4 ? c.x : c.y;
-      const int sh = (i & 3) * 8;
-      const float lo = bf16_bits_to_f32(e2m1_to_bf16_bits((word >> sh) & 0xFu)) * sc;
-      const float hi = bf16_bits_to_f32(e2m1_to_bf16_bits((word >> (sh + 4)) & 0xFu)) * sc;
-      w[i] = (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xFFFF0000u);  // exact
+      w[i] = hmul2_u32(e2m1x2_to_f16x2((word >> ((i & 3) * 8)) & 0xFFu), s2);  // exact
     }
   } else if (src <= -2) {
     const int64_t wr = (int64_t)b * a.swa_cap + (-2 - src);
@@ -80,9 +108,9 @@ __device__ __forceinline__ void dequant_group(const AttnArgs& a, int b, int64_t 
     for (int i = 0; i < 8; ++i) {
       const uint32_t word = cw[i >> 1];
       const int sh = (i & 1) * 16;
-      const float lo = e4m3_to_f32((word >> sh) & 0xFFu) * sc;
-      const float hi = e4m3_to_f32((word >> (sh + 8)) & 0xFFu) * sc;
-      w[i] = f32_to_bf16_bits(lo) | (f32_to_bf16_bits(hi) << 16);
+      const float lo = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32((word >> sh) & 0xFFu) * sc));
+      const float hi = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32((word >> (sh + 8)) & 0xFFu) * sc));
+      w[i] = f32_to_f16_bits(lo) | (f32_to_f16_bits(hi) << 16);
     }
   } else {
 #pragma unroll
@@ -99,7 +127,8 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   AttnSmem<D>& sm = *reinterpret_cast<AttnSmem<D>*>(smem_raw);
   constexpr int QS = AttnSmem<D>::QS, PS = AttnSmem<D>::PS;
-  constexpr int NT = D / 32;           // 8-wide value n-tiles per warp (D/4 channels)
+  constexpr int DW = D / kAttnWarps;   // value channels per warp
+  constexpr int NT = DW / 8;           // 8-wide n-tiles per warp
   const int64_t row = blockIdx.y;
   const int hg = blockIdx.x;
   const int b = (int)(row / a.Tq);
@@ -107,7 +136,7 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
   const int g = lane >> 2, t4 = lane & 3;
 
   const int t = a.q_pos[row];
-  const int nv = n_visible(a.n_entries[b], t);  // only bounds the indices checked below
+  const int nv = n_visible(a.n_entries[b], t);  // bounds the indices checked below
   int n_sel = a.cnt[row];
   if (n_sel < 0 || n_sel > a.K) {
     if (tid == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
@@ -119,12 +148,21 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
   const int n_win = max(0, w_hi - w_lo + 1);
   const int n_keys = n_sel + n_win;
 
-  // Q rows of this head group (zero rows past Hq)
+  // Q rows of this head group as fp16 (zero rows past Hq)
   for (int i = tid; i < kHG * (D / 8); i += kAttnThreads) {
     const int h = i / (D / 8), c8 = i % (D / 8);
     const int head = hg * kHG + h;
     uint4 v = make_uint4(0, 0, 0, 0);
-    if (head < a.Hq) v = *reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + head) * D + c8 * 8);
+    if (head < a.Hq) {
+      const uint4 qb = *reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + head) * D + c8 * 8);
+      const uint32_t qw[4] = {qb.x, qb.y, qb.z, qb.w};
+      uint32_t ov[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ov[j] = f32_to_f16_bits(bf16_bits_to_f32(qw[j] & 0xFFFFu)) |
+                (f32_to_f16_bits(bf16_bits_to_f32(qw[j] >> 16)) << 16);
+      v = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+    }
     *reinterpret_cast<uint4*>(&sm.q[h * QS + c8 * 8]) = v;
   }
   if (tid < kHG) {
@@ -158,70 +196,61 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
       dequant_group<D>(a, b, sm.key_src[kr], grp, &sm.k[kr * QS + grp * 16]);
     }
     __syncthreads();
-    // ---- S = Q K^T : warp owns keys 16*warp .. +15
+    // ---- S = Q K^T : warp owns keys 8*warp .. +7
     {
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      float s0[4] = {0.f, 0.f, 0.f, 0.f};
       const uint32_t qa = smem_u32(&sm.q[(lane & 15) * QS + (lane >> 4) * 8]);
-      const int mi = lane >> 3, r8 = lane & 7;
-      const uint32_t kb = smem_u32(&sm.k[(warp * 16 + (mi >> 1) * 8 + r8) * QS + (mi & 1) * 8]);
+      // x4 over keys 8w..8w+7: matrices = 8-channel chunks 0..3 of a 32-channel step
+      const uint32_t kb = smem_u32(&sm.k[(warp * 8 + (lane & 7)) * QS + (lane >> 3) * 8]);
 #pragma unroll 4
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-        ldsm_x4(qa + ks * 32, a0, a1, a2, a3);
-        ldsm_x4(kb + ks * 32, b0, b1, b2, b3);
-        mma16816(s0, a0, a1, a2, a3, b0, b1);
-        mma16816(s1, a0, a1, a2, a3, b2, b3);
+      for (int ks = 0; ks < D / 32; ++ks) {
+        uint32_t a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3;
+        ldsm_x4(qa + ks * 64, a0, a1, a2, a3);
+        ldsm_x4(qa + ks * 64 + 32, a4, a5, a6, a7);
+        ldsm_x4(kb + ks * 64, b0, b1, b2, b3);
+        mma_f16(s0, a0, a1, a2, a3, b0, b1);
+        mma_f16(s0, a4, a5, a6, a7, b2, b3);
       }
-      const int key0 = warp * 16 + 2 * t4;
-      const bool v00 = sm.key_src[key0] != -1, v01 = sm.key_src[key0 + 1] != -1;
-      const bool v10 = sm.key_src[key0 + 8] != -1, v11 = sm.key_src[key0 + 9] != -1;
-      sm.s[g * kTK + key0] = v00 ? s0[0] * sl2 : -INFINITY;
-      sm.s[g * kTK + key0 + 1] = v01 ? s0[1] * sl2 : -INFINITY;
-      sm.s[(g + 8) * kTK + key0] = v00 ? s0[2] * sl2 : -INFINITY;
-      sm.s[(g + 8) * kTK + key0 + 1] = v01 ? s0[3] * sl2 : -INFINITY;
-      sm.s[g * kTK + key0 + 8] = v10 ? s1[0] * sl2 : -INFINITY;
-      sm.s[g * kTK + key0 + 9] = v11 ? s1[1] * sl2 : -INFINITY;
-      sm.s[(g + 8) * kTK + key0 + 8] = v10 ? s1[2] * sl2 : -INFINITY;
-      sm.s[(g + 8) * kTK + key0 + 9] = v11 ? s1[3] * sl2 : -INFINITY;
+      const int key0 = warp * 8 + 2 * t4;
+      const bool v0 = sm.key_src[key0] != -1, v1 = sm.key_src[key0 + 1] != -1;
+      sm.s[g * kTK + key0] = v0 ? s0[0] * sl2 : -INFINITY;
+      sm.s[g * kTK + key0 + 1] = v1 ? s0[1] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0] = v0 ? s0[2] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0 + 1] = v1 ? s0[3] * sl2 : -INFINITY;
     }
     __syncthreads();
-    // ---- online softmax: 8 threads per head, 8 keys each
+    // ---- online softmax: 16 threads per head, 4 keys each
     {
-      const int h = tid >> 3, part = tid & 7;
-      float sv[8];
-      float mx = -INFINITY;
+      const int h = tid >> 4, part = tid & 15;
+      const float4 sv = *reinterpret_cast<const float4*>(&sm.s[h * kTK + part * 4]);
+      float mx = fmaxf(fmaxf(sv.x, sv.y), fmaxf(sv.z, sv.w));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        sv[i] = sm.s[h * kTK + part * 8 + i];
-        mx = fmaxf(mx, sv[i]);
-      }
-#pragma unroll
-      for (int o2 = 1; o2 < 8; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
       const float m_old = sm.m[h];
       const float m_new = fmaxf(m_old, mx);
-      float sum = 0.f;
-      uint32_t pw[4];
+      const bool none = m_new == -INFINITY;
+      const __half p0 = __float2half_rn(none ? 0.f : exp2f(sv.x - m_new));
+      const __half p1 = __float2half_rn(none ? 0.f : exp2f(sv.y - m_new));
+      const __half p2 = __float2half_rn(none ? 0.f : exp2f(sv.z - m_new));
+      const __half p3 = __float2half_rn(none ? 0.f : exp2f(sv.w - m_new));
+      // normalise by the rounded weights that the PV product uses
+      float sum = __half2float(p0) + __half2float(p1) + __half2float(p2) + __half2float(p3);
+      uint2 pw;
+      pw.x = (uint32_t)__half_as_ushort(p0) | ((uint32_t)__half_as_ushort(p1) << 16);
+      pw.y = (uint32_t)__half_as_ushort(p2) | ((uint32_t)__half_as_ushort(p3) << 16);
+      *reinterpret_cast<uint2*>(&sm.p[h * PS + part * 4]) = pw;
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {
-        const float p0 = m_new == -INFINITY ? 0.f : exp2f(sv[i] - m_new);
-        const float p1 = m_new == -INFINITY ? 0.f : exp2f(sv[i + 1] - m_new);
-        const uint32_t b0 = f32_to_bf16_bits(p0), b1 = f32_to_bf16_bits(p1);
-        sum += bf16_bits_to_f32(b0) + bf16_bits_to_f32(b1);  // normalise by what PV uses
-        pw[i >> 1] = b0 | (b1 << 16);
-      }
-      *reinterpret_cast<uint4*>(&sm.p[h * PS + part * 8]) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-#pragma unroll
-      for (int o2 = 1; o2 < 8; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+      for (int o2 = 1; o2 < 16; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
       __syncwarp();
       if (part == 0) {
-        const float al = (m_new == -INFINITY) ? 1.f : exp2f(m_old - m_new);
+        const float al = none ? 1.f : exp2f(m_old - m_new);
         sm.alpha[h] = al;
         sm.l[h] = sm.l[h] * al + sum;
         sm.m[h] = m_new;
       }
     }
     __syncthreads();
-    // ---- O = O * alpha + P V : warp owns channels warp*(D/4) .. +D/4
+    // ---- O = O * alpha + P V : warp owns channels warp*DW .. +DW
     {
       const float al0 = sm.alpha[g], al1 = sm.alpha[g + 8];
 #pragma unroll
@@ -234,13 +263,18 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
       for (int kk = 0; kk < kTK / 16; ++kk) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(pa + kk * 32, a0, a1, a2, a3);
-        const uint32_t vb = smem_u32(&sm.k[(kk * 16 + (mi & 1) * 8 + r8) * QS + warp * (D / 4) + (mi >> 1) * 8]);
+        const uint32_t vb = smem_u32(&sm.k[(kk * 16 + (mi & 1) * 8 + r8) * QS + warp * DW + (mi >> 1) * 8]);
 #pragma unroll
         for (int np = 0; np < NT / 2; ++np) {
           uint32_t b0, b1, b2, b3;
           ldsm_x4_t(vb + np * 32, b0, b1, b2, b3);
-          mma16816(o[2 * np], a0, a1, a2, a3, b0, b1);
-          mma16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+          mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
+          mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+        if (NT & 1) {
+          uint32_t b0, b1;
+          ldsm_x2_t(smem_u32(&sm.k[(kk * 16 + (lane & 15)) * QS + warp * DW + (NT - 1) * 8]), b0, b1);
+          mma_f16(o[NT - 1], a0, a1, a2, a3, b0, b1);
         }
       }
     }
@@ -253,7 +287,7 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
   const int head0 = hg * kHG + g, head1 = head0 + 8;
 #pragma unroll
   for (int i = 0; i < NT; ++i) {
-    const int ch = warp * (D / 4) + i * 8 + 2 * t4;
+    const int ch = warp * DW + i * 8 + 2 * t4;
     if (head0 < a.Hq)
       *reinterpret_cast<float2*>(a.O + (row * a.Hq + head0) * D + ch) = make_float2(o[i][0] * inv0, o[i][1] * inv0);
     if (head1 < a.Hq)

@@ -11,6 +11,7 @@
 // CTA tiles, cp.async double buffering.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace csa2 {
 
@@ -137,11 +138,139 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
     }
 }
 
+// ---- tcgen05 path ----------------------------------------------------------------
+// CTA tile 128 (M) x 128 (N) x 64 (K) per stage, 4-stage ring of operands in the
+// 128-byte-swizzled K-major layout (8-row atoms of 1024 B, 16-byte chunk index
+// XOR row % 8) written by cp.async; thread 0 issues tcgen05.mma (M=128, N=128,
+// K=16) into a 128-column fp32 TMEM accumulator and commits each stage to an
+// mbarrier that frees its buffers.  Every wait is bounded.
+constexpr int kTcM = 128, kTcN = 128, kTcK = 64, kTcStages = 4, kTcThreads = 128;
+constexpr int kTcStageBytes = (kTcM + kTcN) * kTcK * 2;   // 32 KB
+
+__global__ void __launch_bounds__(kTcThreads)
+k_compress_gemm_tc(const uint16_t* __restrict__ hidden, int G, int T, int H, const uint16_t* __restrict__ W,
+                   int d, const uint16_t* __restrict__ W_idx, int Di, int M, int k_per_split,
+                   float* __restrict__ partials, uint32_t* status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t bar_free[kTcStages];
+  __shared__ uint64_t bar_done;
+  __shared__ uint32_t tmem_slot;
+  const uint32_t pad = (1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u;
+  unsigned char* ring = smem_raw + pad;
+  const int N = d + Di;
+  const int64_t Kd = 4LL * H;
+  const int m0 = blockIdx.y * kTcM, n0 = blockIdx.x * kTcN;
+  const int kbeg = blockIdx.z * k_per_split;
+  const int n_iter = k_per_split / kTcK;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < kTcStages; ++i) tc::mbar_init(&bar_free[i], 1);
+    tc::mbar_init(&bar_done, 1);
+    tc::mbar_fence_init();
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcN);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  // row sources: this thread copies rows (tid / 8) + 16 i, 16-byte chunk tid % 8
+  const int c16 = tid & 7;
+  auto stage_ptr = [&](int st) { return ring + st * kTcStageBytes; };
+  auto issue_loads = [&](int st, int k0) {
+    unsigned char* sa = stage_ptr(st);
+    unsigned char* sb = sa + kTcM * kTcK * 2;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = (tid >> 3) + 16 * i;
+      const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((c16 ^ (r & 7)) << 4);
+      const int m = m0 + r;
+      const bool okA = m < M;
+      const int mm = okA ? m : 0;
+      const uint16_t* ga = hidden + ((int64_t)(mm / G) * T + 4LL * (mm % G)) * H + k0 + c16 * 8;
+      const int n = n0 + r;
+      const bool okB = n < N;
+      const uint16_t* gb = !okB ? W : (n < d ? W + (int64_t)n * Kd : W_idx + (int64_t)(n - d) * Kd);
+      gb += okB ? k0 + c16 * 8 : 0;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_addr(sa + off)), "l"(ga),
+                   "r"(okA ? 16 : 0));
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_addr(sb + off)), "l"(gb),
+                   "r"(okB ? 16 : 0));
+    }
+    asm volatile("cp.async.commit_group;\n");
+  };
+
+  constexpr uint32_t idesc = tc::idesc_f16(kTcM, kTcN, 1, 0, 0);
+  bool ok = true;
+  // prologue: stages 0 .. S-2
+  for (int i = 0; i < kTcStages - 1; ++i) {
+    if (i < n_iter) issue_loads(i, kbeg + i * kTcK);
+    else asm volatile("cp.async.commit_group;\n");
+  }
+  for (int it = 0; it < n_iter; ++it) {
+    // refill the stage that chunk it + S - 1 goes to, once its previous MMA is done;
+    // the block votes so that every thread takes the same branch after a timeout
+    const int nxt = it + kTcStages - 1;
+    bool okw = true;
+    if (nxt < n_iter && nxt >= kTcStages) okw = tc::mbar_wait(&bar_free[nxt % kTcStages], ((nxt / kTcStages) - 1) & 1);
+    ok = __syncthreads_and(okw) != 0;
+    if (!ok) break;
+    if (nxt < n_iter) issue_loads(nxt % kTcStages, kbeg + nxt * kTcK);
+    else asm volatile("cp.async.commit_group;\n");
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kTcStages - 1));
+    tc::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc::tc_fence_after();
+      const int st = it % kTcStages;
+      const uint32_t sa = tc::smem_addr(stage_ptr(st));
+      const uint32_t sb = sa + kTcM * kTcK * 2;
+#pragma unroll
+      for (int ks = 0; ks < kTcK / 16; ++ks) {
+        const uint64_t ad = tc::smem_desc(sa + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
+        const uint64_t bd = tc::smem_desc(sb + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
+        tc::mma_f16(tmem, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&bar_free[st]);
+      if (it == n_iter - 1) tc::mma_commit(&bar_done);
+    }
+  }
+  asm volatile("cp.async.wait_group 0;\n");
+  if (ok && n_iter > 0) ok = __syncthreads_and(tc::mbar_wait(&bar_done, 0)) != 0;
+  if (!ok && tid == 0) raise_status(status, CSA2_STATUS_TIMEOUT);
+  tc::tc_fence_after();
+  if (ok && n_iter > 0) {
+    // epilogue: lane (32 warp + lane) holds row m0 + 32 warp + lane
+    const int m = m0 + warp * 32 + lane;
+    float* out = partials + (int64_t)blockIdx.z * M * N + (int64_t)m * N + n0;
+#pragma unroll 1
+    for (int c = 0; c < kTcN; c += 16) {
+      float v[16];
+      tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c, v);
+      tc::tmem_wait_ld();
+      if (m < M) {
+#pragma unroll
+        for (int q = 0; q < 16; q += 4)
+          if (n0 + c + q < N) *reinterpret_cast<float4*>(out + c + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, kTcN);
+}
+
+// The tensor-memory GEMM is used once its operand layout has been checked on
+// the GPU; the mma.sync kernel stays for shapes it does not take.
+constexpr bool kUseTcCompress = false;
+
 static int compress_splits(int M, int N, int Kd) {
   const int tiles = ((M + kGM - 1) / kGM) * ((N + kGN - 1) / kGN);
   int splits = 1;
-  // aim for >= 2 waves of 152 SMs while each split keeps >= 512 of K
-  while (tiles * splits < 304 && Kd / (splits * 2) >= 512 && (Kd / (splits * 2)) % kGK == 0) splits *= 2;
+  // aim for about one wave of 152 SMs while each split keeps >= 1024 of K
+  // (a multiple of the 64-wide K stage of both kernels)
+  while (tiles * splits < 152 && Kd / (splits * 2) >= 1024 && (Kd / (splits * 2)) % 64 == 0) splits *= 2;
   return splits;
 }
 
@@ -158,6 +287,14 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
   const int G = T / 4, M = B * G, N = d + (W_idx ? Di : 0), Kd = 4 * H;
   if (M == 0) return cudaSuccess;
   dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
+  if (kUseTcCompress && (Kd / n_split) % kTcK == 0) {
+    const size_t smem = kTcStages * kTcStageBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_compress_gemm_tc<<<grid, kTcThreads, smem, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M,
+                                                      Kd / n_split, partials, status_word());
+    return counted(cudaGetLastError());
+  }
   k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M,
                                              Kd / n_split, partials);
   return counted(cudaGetLastError());

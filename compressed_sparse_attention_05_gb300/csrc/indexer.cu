@@ -81,12 +81,26 @@ __device__ __forceinline__ void load_query(const uint16_t* __restrict__ q, const
   }
 }
 
+// Order-preserving key of an fp32 score (-0 folded into +0); its top 11 bits
+// index the per-row histogram the Top-K kernel starts from.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7FFFFFFFu) == 0) u = 0;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+constexpr int kHistBins = 2048;
+constexpr int kHistMaxQG = 8;   // query rows per CTA when a histogram is built
+
 // Full mode.  grid = (entry chunks, query groups, B); a CTA scores one chunk
 // of kIdxChunk entries of sequence b against QG consecutive query tokens.
+// Each warp walks its 16-entry tiles with the next tile's key fragments in
+// flight while the current one is on the tensor cores.
 template <int NCH, int NT>
 __global__ void __launch_bounds__(kIdxWarps * 32)
 k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t stride,
-                   float* __restrict__ blockmax, int64_t bm_stride, uint32_t* status) {
+                   float* __restrict__ blockmax, int64_t bm_stride, uint32_t* __restrict__ hist,
+                   uint32_t* status) {
+  extern __shared__ uint32_t shist[];   // [QG][kHistBins] when hist != nullptr
   const int b = blockIdx.z;
   const int i0 = blockIdx.y * QG;
   const int i1 = min(a.Tq, i0 + QG);
@@ -95,48 +109,91 @@ k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t st
   for (int i = i0; i < i1; ++i) max_vis = max(max_vis, n_visible(n_ent, a.q_pos[(int64_t)b * a.Tq + i]));
   const int chunk0 = blockIdx.x * kIdxChunk;
   if (chunk0 >= max_vis) return;
+  if (hist) {
+    for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) shist[i] = 0;
+    __syncthreads();
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const uint16_t* kbase = reinterpret_cast<const uint16_t*>(a.k);
-  for (int tt = 0; tt < kIdxTilesPerWarp; ++tt) {
-    const int e0 = chunk0 + (warp * kIdxTilesPerWarp + tt) * 16;
-    if (e0 >= max_vis) break;
+  const int tile0 = chunk0 + warp * kIdxTilesPerWarp * 16;
+  uint4 ka[2][NCH], kb[2][NCH];
+  auto load_tile = [&](int e0, uint4 (&ra)[NCH], uint4 (&rb)[NCH]) -> bool {
     const int64_t slot0 = entry_slot(a.page_table, a.max_pages, a.n_pages, b, e0, status);
-    if (slot0 < 0) continue;
-    uint4 ka[NCH], kb[NCH];
+    if (slot0 < 0) return false;
     const uint16_t* rg = kbase + (slot0 + g) * a.Di + 8 * t;
     const uint16_t* rg8 = kbase + (slot0 + g + 8) * a.Di + 8 * t;
 #pragma unroll
     for (int c = 0; c < NCH; ++c) {
-      ka[c] = __ldg(reinterpret_cast<const uint4*>(rg + 32 * c));
-      kb[c] = __ldg(reinterpret_cast<const uint4*>(rg8 + 32 * c));
+      ra[c] = __ldg(reinterpret_cast<const uint4*>(rg + 32 * c));
+      rb[c] = __ldg(reinterpret_cast<const uint4*>(rg8 + 32 * c));
     }
-    for (int i = i0; i < i1; ++i) {
-      const int64_t row = (int64_t)b * a.Tq + i;
-      const int nv = n_visible(n_ent, a.q_pos[row]);
-      if (e0 >= nv) continue;
-      uint4 qf[NT][NCH];
-      float wv[NT][2];
-      load_query<NCH, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi,
-                          a.Hi, a.Di, lane, qf, wv);
-      float sg, sg8;
-      tile_scores<NCH, NT>(ka, kb, qf, wv, sg, sg8);
-      const bool vg = e0 + g < nv, vg8 = e0 + g + 8 < nv;
-      if (t == 0 && vg) scores[row * stride + e0 + g] = sg;
-      if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
-      if (blockmax) {
-        float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;
+    return true;
+  };
+  bool ok_cur = tile0 < max_vis && load_tile(tile0, ka[0], kb[0]);
 #pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-          m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-          m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+  for (int tt = 0; tt < kIdxTilesPerWarp; ++tt) {
+    const int cur = tt & 1;
+    const int e0 = tile0 + tt * 16;
+    if (e0 >= max_vis) break;
+    bool ok_next = false;
+    if (tt + 1 < kIdxTilesPerWarp && e0 + 16 < max_vis) ok_next = load_tile(e0 + 16, ka[cur ^ 1], kb[cur ^ 1]);
+    if (ok_cur) {
+      for (int i = i0; i < i1; ++i) {
+        const int64_t row = (int64_t)b * a.Tq + i;
+        const int nv = n_visible(n_ent, a.q_pos[row]);
+        if (e0 >= nv) continue;
+        uint4 qf[NT][NCH];
+        float wv[NT][2];
+        load_query<NCH, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi,
+                            a.Hi, a.Di, lane, qf, wv);
+        float sg, sg8;
+        tile_scores<NCH, NT>(ka[cur], kb[cur], qf, wv, sg, sg8);
+        const bool vg = e0 + g < nv, vg8 = e0 + g + 8 < nv;
+        if (t == 0 && vg) scores[row * stride + e0 + g] = sg;
+        if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
+        if (hist) {
+          // lanes t == 0 carry entry g, lanes t == 1 entry g + 8
+          const bool has = (t == 0 && vg) || (t == 1 && vg8);
+          const uint32_t bin = has ? score_key(t == 0 ? sg : sg8) >> 21 : 0xFFFFFFFFu;
+          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+          if (has && lane == __ffs(peers) - 1) atomicAdd(&shist[(i - i0) * kHistBins + bin], __popc(peers));
         }
-        if (lane == 0) blockmax[row * bm_stride + e0 / 8] = m0;
-        if (lane == 1 && e0 + 8 < nv) blockmax[row * bm_stride + e0 / 8 + 1] = m1;
+        if (blockmax) {
+          float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+            m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+          }
+          if (lane == 0) blockmax[row * bm_stride + e0 / 8] = m0;
+          if (lane == 1 && e0 + 8 < nv) blockmax[row * bm_stride + e0 / 8 + 1] = m1;
+        }
       }
     }
+    ok_cur = ok_next;
   }
+  if (hist) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) {
+      const uint32_t c = shist[i];
+      if (c) atomicAdd(&hist[((int64_t)b * a.Tq + i0 + i / kHistBins) * kHistBins + (i % kHistBins)], c);
+    }
+  }
+}
+
+// Histogram of already-written scores (the generic scoring path).
+__global__ void k_score_hist(const float* __restrict__ scores, int64_t stride, IndexerArgs a,
+                             uint32_t* __restrict__ hist) {
+  const int64_t row = blockIdx.y;
+  const int b = (int)(row / a.Tq);
+  const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[row]);
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const bool has = j < nv;
+  const uint32_t bin = has ? score_key(scores[row * stride + j]) >> 21 : 0xFFFFFFFFu;
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  if (has && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[row * kHistBins + bin], __popc(peers));
 }
 
 // Reindex.  grid = (pool-block pairs / kIdxWarps, rows): warp w scores the
@@ -250,12 +307,19 @@ static bool mma_path(const IndexerArgs& a) {
 
 template <int NCH, int NT>
 static cudaError_t launch_full_mma(const IndexerArgs& a, float* scores, int64_t stride,
-                                   float* blockmax, int64_t bm_stride, int max_entries,
+                                   float* blockmax, int64_t bm_stride, int max_entries, uint32_t* hist,
                                    cudaStream_t s) {
-  const int QG = a.Tq >= 16 ? 16 : a.Tq;
+  const int qg_max = hist ? kHistMaxQG : 16;
+  const int QG = a.Tq >= qg_max ? qg_max : a.Tq;
+  const size_t smem = hist ? (size_t)QG * kHistBins * sizeof(uint32_t) : 0;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_index_scores_mma<NCH, NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
   dim3 grid((max_entries + kIdxChunk - 1) / kIdxChunk, (a.Tq + QG - 1) / QG, a.B);
-  k_index_scores_mma<NCH, NT><<<grid, kIdxWarps * 32, 0, s>>>(a, QG, scores, stride, blockmax,
-                                                              bm_stride, status_word());
+  k_index_scores_mma<NCH, NT><<<grid, kIdxWarps * 32, smem, s>>>(a, QG, scores, stride, blockmax,
+                                                                 bm_stride, hist, status_word());
   return counted(cudaGetLastError());
 }
 
@@ -279,10 +343,10 @@ static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, co
   } while (0)
 
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
-                                int64_t bm_stride, int block, int max_entries, cudaStream_t s) {
+                                int64_t bm_stride, int block, int max_entries, uint32_t* hist, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0 || max_entries == 0) return cudaSuccess;
   if (mma_path(a) && block == 8) {
-    CSA2_DISPATCH_MMA(launch_full_mma, a, scores, stride, blockmax, bm_stride, max_entries, s);
+    CSA2_DISPATCH_MMA(launch_full_mma, a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
   }
   dim3 grid((max_entries + 255) / 256, a.B * a.Tq);
   const size_t smem = (size_t)(a.Hi * a.Di + a.Hi) * sizeof(float);
@@ -293,7 +357,14 @@ cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t str
     k_index_scores_generic<float><<<grid, 256, smem, s>>>(a, nullptr, nullptr, 0, scores, stride,
                                                            nullptr, status_word());
   cudaError_t e = counted(cudaGetLastError());
-  if (e != cudaSuccess || !blockmax) return e;
+  if (e != cudaSuccess) return e;
+  if (hist) {
+    dim3 hg((max_entries + 255) / 256, a.B * a.Tq);
+    k_score_hist<<<hg, 256, 0, s>>>(scores, stride, a, hist);
+    e = counted(cudaGetLastError());
+    if (e != cudaSuccess) return e;
+  }
+  if (!blockmax) return cudaSuccess;
   ValidSpec v{nullptr, a.n_entries, a.q_pos, a.Tq, 1, a.max_entries};
   return launch_block_max(scores, (int64_t)a.B * a.Tq, stride, v, block, blockmax, bm_stride, s);
 }

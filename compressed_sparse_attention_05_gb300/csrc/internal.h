@@ -66,10 +66,11 @@ struct IndexerArgs {
   int64_t n_pages;
   int max_entries;           // visible counts are clamped to this (buffer bound)
 };
-// Full: scores[row][j] for visible j; blockmax (nullable) per `block` entries.
+// Full: scores[row][j] for visible j; blockmax (nullable) per `block` entries;
+// hist (nullable, zeroed by the caller): per-row 2048-bin key histogram for launch_topk.
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride,
                                 float* blockmax, int64_t bm_stride, int block, int max_entries,
-                                cudaStream_t s);
+                                uint32_t* hist, cudaStream_t s);
 // Reindex: compact scores[row][p*block + e] of the pooled blocks' visible
 // positions; n_valid[row] receives the compact count.
 cudaError_t launch_index_scores_pool(const IndexerArgs& a, const int32_t* pool,
@@ -95,8 +96,11 @@ struct Remap {
   int64_t pool_stride;
   int block;
 };
+// hist (nullable): per-row 2048-bin histogram of the top 11 bits of the
+// order-preserving score keys of the valid columns (built by the scoring kernel).
 cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
-                        int32_t* out_idx, int32_t* out_cnt, Remap remap, cudaStream_t s);
+                        int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
+                        int64_t hist_stride, cudaStream_t s);
 // Block maxima of the valid columns: out[row][b] = max(scores[row][block*b ..]).
 cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, ValidSpec v,
                              int block, float* out, int64_t out_stride, cudaStream_t s);

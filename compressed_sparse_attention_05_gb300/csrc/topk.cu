@@ -1,15 +1,20 @@
-// Top-K selection (radix select) and block maxima for the hierarchical pool.
+// Top-K selection and block maxima for the hierarchical pool.
 //
 // "DeepSeek-V4.1 架构解析" §02: each query keeps the Top-512 entries by index
 // score; the hierarchical indexer keeps the 2,048 blocks of 8 with the largest
 // block-max score.  Tie and ordering rules: readings R8-R9 of include/csa2.h.
 //
 // One CTA per row.  Scores map to order-preserving 32-bit keys (-0 folded into
-// +0); four 8-bit radix passes find the exact K-th key T and how many of the
-// entries equal to T are taken; a last pass in index order writes the
-// selection ascending, taking equal keys from the lowest index up.  Every
-// pass reads the row once with coalesced loads; histogram updates are
-// aggregated per warp with match.any so equal digits cost one shared atomic.
+// +0).  A 2048-bin histogram of the top 11 key bits (built by the scoring
+// kernel while it writes the scores, or here in one pass) locates the bin
+// that holds the K-th key; one pass over the row then keeps every entry of a
+// higher bin and copies the entries of that bin into shared memory, where the
+// exact K-th key and its tie count are found by radix passes over the few
+// candidates.  The selection is sorted by index in shared memory and written
+// ascending.  When the threshold bin is too full for shared memory (e.g. many
+// equal scores), a radix select over the whole row finishes from the 11-bit
+// prefix instead.  Warp-aggregated (match.any / ballot) shared atomics keep
+// equal digits from serialising.
 #include "common.cuh"
 #include "internal.h"
 
@@ -17,6 +22,8 @@ namespace csa2 {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kCandCap = 4096;      // candidates of the threshold bin kept in smem
+constexpr int kSelCap = 4096;       // largest K
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -28,6 +35,7 @@ __device__ __forceinline__ int row_valid(const ValidSpec& v, int64_t row, int64_
   int64_t n;
   if (v.n_valid) {
     n = v.n_valid[row];
+    if (v.divisor > 1) n = (n + v.divisor - 1) / v.divisor;
   } else if (v.n_entries) {
     const int b = (int)(row / v.Tq);
     int ne = v.n_entries[b];
@@ -45,8 +53,8 @@ __device__ __forceinline__ int32_t remap_index(const Remap& r, int64_t row, int 
   return r.pool[row * r.pool_stride + c / r.block] * r.block + c % r.block;
 }
 
-// Exclusive block-wide prefix sum of one int per thread (kTopkThreads threads).
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& total) {
+// Exclusive block-wide prefix sum of one int per thread.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -63,28 +71,99 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& t
       int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < kTopkWarps) warp_tot[lane] = w;  // inclusive warp totals
+    if (lane < kTopkWarps) warp_tot[lane] = w;
   }
   __syncthreads();
   const int before = warp ? warp_tot[warp - 1] : 0;
-  total = warp_tot[kTopkWarps - 1];
   __syncthreads();
   return before + x - v;
 }
 
+// Adds `digit` (< nbins, or >= nbins for "none") to a shared histogram with
+// one atomic per distinct digit of the warp.
+__device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, uint32_t nbins) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+  if (digit < nbins && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[digit], __popc(peers));
+}
+
+// Slot in a shared list for every lane with `take` (one atomic per warp); -1
+// for lanes that take nothing or when the list is full.
+__device__ __forceinline__ int warp_slot(int* counter, bool take, int cap) {
+  const uint32_t m = __ballot_sync(0xffffffffu, take);
+  if (!m) return -1;
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  if (lane == __ffs(m) - 1) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+  const int pos = base + __popc(m & ((1u << lane) - 1));
+  return (take && pos < cap) ? pos : -1;
+}
+
+// Finds, scanning digits from the top, the digit holding the need-th largest
+// element of a `bins`-bin histogram; *above receives the count in higher bins.
+__device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int need, int* warp_tot, int* above) {
+  __shared__ int s_digit, s_above;
+  const int per = (bins + kTopkThreads - 1) / kTopkThreads;
+  const int hi = bins - (int)threadIdx.x * per;   // thread t owns [hi - per, hi), highest first
+  const int lo = max(0, hi - per);
+  int c = 0;
+  for (int d = lo; d < hi; ++d) c += hist[d];
+  if (threadIdx.x == 0) { s_digit = 0; s_above = 0; }
+  const int before = block_exclusive_scan(c, warp_tot);
+  if (before < need && before + c >= need) {
+    int cum = before;
+    for (int d = hi - 1; d >= lo; --d) {
+      const int h = (int)hist[d];
+      if (cum + h >= need) {
+        s_digit = d;
+        s_above = cum;
+        break;
+      }
+      cum += h;
+    }
+  }
+  __syncthreads();
+  *above = s_above;
+  return s_digit;
+}
+
+// Ascending bitonic sort of n2 (a power of two) 32-bit values in shared memory.
+template <typename T>
+__device__ __forceinline__ void block_bitonic_sort(T* a, int n2) {
+  for (int kb = 2; kb <= n2; kb <<= 1)
+    for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+      for (int i = threadIdx.x; i < n2; i += kTopkThreads) {
+        const int ixj = i ^ jb;
+        if (ixj > i) {
+          const T x = a[i], y = a[ixj];
+          if ((x > y) == ((i & kb) == 0)) { a[i] = y; a[ixj] = x; }
+        }
+      }
+      __syncthreads();
+    }
+}
+
+struct TopkSmem {
+  uint32_t hist[2048];
+  uint32_t hist2[256];
+  int warp_tot[kTopkWarps];
+  int nA, nC, nT;
+  int32_t sel[kSelCap];           // selected indices (unsorted), then sorted
+  uint32_t ckey[kCandCap];        // candidate keys of the threshold bin
+  int32_t cidx[kCandCap];         // and their indices
+};
+
 __global__ void __launch_bounds__(kTopkThreads)
-k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k,
-       int32_t* __restrict__ out_idx, int32_t* __restrict__ out_cnt, Remap remap) {
-  __shared__ uint32_t hist[kTopkWarps][256];
-  __shared__ int warp_tot[kTopkWarps];
-  __shared__ uint32_t sh_prefix;
-  __shared__ int sh_need;
+k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+       int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   const int64_t row = blockIdx.x;
   const float* s = scores + row * stride;
   const int n = row_valid(v, row, stride);
   const int kk = min(k, n);
   int32_t* out = out_idx + row * (int64_t)k;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
 
   for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
   if (tid == 0) out_cnt[row] = kk;
@@ -94,49 +173,122 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k,
     return;
   }
 
-  uint32_t prefix = 0, mask = 0;
-  int need = kk;
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int i = tid; i < kTopkWarps * 256; i += kTopkThreads) (&hist[0][0])[i] = 0;
+  // ---- histogram of the top 11 key bits
+  if (hist_in) {
+    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
+  } else {
+    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
     __syncthreads();
     for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
       const int j = j0 + tid;
-      uint32_t digit = 256;  // 256 = not counted
+      warp_hist_add(sm.hist, j < n ? order_key(s[j]) >> 21 : 0xFFFFFFFFu, 2048);
+    }
+  }
+  if (tid == 0) { sm.nA = 0; sm.nC = 0; sm.nT = 0; }
+  __syncthreads();
+  int above;
+  const int bstar = find_digit(sm.hist, 2048, kk, sm.warp_tot, &above);
+  int need = kk - above;                  // entries of bin bstar to take
+  const int n_bin = (int)sm.hist[bstar];
+
+  if (n_bin <= kCandCap) {
+    // ---- one pass: higher bins -> selected; bin bstar -> candidates
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+      const int j = j0 + tid;
+      uint32_t key = 0, bin = 0;
+      if (j < n) {
+        key = order_key(s[j]);
+        bin = key >> 21;
+      }
+      const int ps = warp_slot(&sm.nA, j < n && bin > (uint32_t)bstar, kSelCap);
+      if (ps >= 0) sm.sel[ps] = j;
+      const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
+      if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
+    }
+    __syncthreads();
+    const int nC = min(sm.nC, kCandCap);
+    // ---- exact threshold among the candidates: 3 radix passes over 21 bits
+    uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
+    for (int p = 0; p < 3; ++p) {
+      const int sh = 14 - 7 * p;
+      const uint32_t nb = 128;
+      for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
+        const int i = i0 + tid;
+        uint32_t dg = 0xFFFFFFFFu;
+        if (i < nC) {
+          const uint32_t key = sm.ckey[i];
+          if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
+        }
+        warp_hist_add(sm.hist2, dg, nb);
+      }
+      __syncthreads();
+      int ab;
+      const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+      need -= ab;
+      prefix |= (uint32_t)dg << sh;
+      mask |= (nb - 1) << sh;
+    }
+    const uint32_t T = prefix;             // exact K-th key; `need` ties at T are taken
+    // candidates above T join the selection; indices of ties at T go to cidx[0..nT)
+    // (written only after every thread has read its candidate of the round)
+    for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
+      const int i = i0 + tid;
+      const bool ok = i < nC;
+      const uint32_t key = ok ? sm.ckey[i] : 0;
+      const int32_t idx = ok ? sm.cidx[i] : 0;
+      __syncthreads();
+      const int ps = warp_slot(&sm.nA, ok && key > T, kSelCap);
+      if (ps >= 0) sm.sel[ps] = idx;
+      const int pt = warp_slot(&sm.nT, ok && key == T, kCandCap);
+      if (pt >= 0) sm.cidx[pt] = idx;
+      __syncthreads();
+    }
+    const int nT = min(sm.nT, kCandCap);
+    // ties: the `need` lowest indices
+    int nt2 = 1;
+    while (nt2 < nT) nt2 <<= 1;
+    for (int i = nT + tid; i < nt2; i += kTopkThreads) sm.cidx[i] = 0x7FFFFFFF;
+    __syncthreads();
+    block_bitonic_sort(sm.cidx, nt2);
+    const int base = min(sm.nA, kSelCap);
+    for (int i = tid; i < need && i < nT && base + i < kSelCap; i += kTopkThreads) sm.sel[base + i] = sm.cidx[i];
+    __syncthreads();
+    // sort the kk selected indices ascending and write them
+    int n2 = 1;
+    while (n2 < kk) n2 <<= 1;
+    for (int i = kk + tid; i < n2; i += kTopkThreads) sm.sel[i] = 0x7FFFFFFF;
+    __syncthreads();
+    block_bitonic_sort(sm.sel, n2);
+    for (int i = tid; i < kk; i += kTopkThreads) out[i] = remap_index(remap, row, sm.sel[i]);
+    return;
+  }
+
+  // ---- crowded threshold bin: radix select over the row from the 11-bit prefix
+  uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
+  for (int p = 0; p < 3; ++p) {
+    const int sh = p == 0 ? 13 : (p == 1 ? 5 : 0);
+    const uint32_t nb = p == 2 ? 32u : 256u;
+    for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
+    __syncthreads();
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+      const int j = j0 + tid;
+      uint32_t dg = 0xFFFFFFFFu;
       if (j < n) {
         const uint32_t key = order_key(s[j]);
-        if ((key & mask) == prefix) digit = (key >> shift) & 0xFFu;
+        if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
       }
-      const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-      if (digit < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[warp][digit], __popc(peers));
+      warp_hist_add(sm.hist2, dg, nb);
     }
     __syncthreads();
-    if (tid < 256) {
-      uint32_t c = 0;
-#pragma unroll 8
-      for (int w = 0; w < kTopkWarps; ++w) c += hist[w][tid];
-      hist[0][tid] = c;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      int cum = 0;
-      for (int dg = 255; dg >= 0; --dg) {
-        const int c = (int)hist[0][dg];
-        if (cum + c >= need) {
-          sh_prefix = prefix | ((uint32_t)dg << shift);
-          sh_need = need - cum;
-          break;
-        }
-        cum += c;
-      }
-    }
-    __syncthreads();
-    prefix = sh_prefix;
-    need = sh_need;
-    mask |= 0xFFu << shift;
+    int ab;
+    const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+    need -= ab;
+    prefix |= (uint32_t)dg << sh;
+    mask |= (nb - 1) << sh;
   }
-  const uint32_t T = prefix;  // the K-th largest key; `need` of the keys == T are taken
-
+  const uint32_t T = prefix;
   // index-ordered output: thread tid owns columns [lo, hi)
   const int chunk = (n + kTopkThreads - 1) / kTopkThreads;
   const int lo = min(n, tid * chunk), hi = min(n, lo + chunk);
@@ -146,17 +298,20 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k,
     gt += key > T;
     eq += key == T;
   }
-  int tot;
-  const int gt_before = block_exclusive_scan(gt, warp_tot, tot);
-  const int eq_before = block_exclusive_scan(eq, warp_tot, tot);
+  const int gt_before = block_exclusive_scan(gt, sm.warp_tot);
+  const int eq_before = block_exclusive_scan(eq, sm.warp_tot);
   int pos = gt_before + min(eq_before, need);
   int eq_seen = eq_before;
   for (int j = lo; j < hi; ++j) {
     const uint32_t key = order_key(s[j]);
     if (key > T) {
-      out[pos++] = remap_index(remap, row, j);
+      if (pos < kk) out[pos] = remap_index(remap, row, j);
+      ++pos;
     } else if (key == T) {
-      if (eq_seen < need) out[pos++] = remap_index(remap, row, j);
+      if (eq_seen < need) {
+        if (pos < kk) out[pos] = remap_index(remap, row, j);
+        ++pos;
+      }
       ++eq_seen;
     }
   }
@@ -179,9 +334,14 @@ __global__ void k_block_max(const float* __restrict__ scores, int64_t stride, Va
 }
 
 cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
-                        int32_t* out_idx, int32_t* out_cnt, Remap remap, cudaStream_t s) {
+                        int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
+                        int64_t hist_stride, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
-  k_topk<<<(unsigned)rows, kTopkThreads, 0, s>>>(scores, stride, v, k, out_idx, out_cnt, remap);
+  const size_t smem = sizeof(TopkSmem);
+  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_topk<<<(unsigned)rows, kTopkThreads, smem, s>>>(scores, stride, v, k, out_idx, out_cnt, remap, hist,
+                                                    hist_stride);
   return counted(cudaGetLastError());
 }
 

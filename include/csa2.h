@@ -114,6 +114,7 @@ extern "C" {
 #define CSA2_STATUS_BAD_PAGE 1u     /* page-table entry outside [0, n_pages)  */
 #define CSA2_STATUS_BAD_INDEX 2u    /* an index outside the visible entries   */
 #define CSA2_STATUS_BAD_COUNT 4u    /* a count or position out of range       */
+#define CSA2_STATUS_TIMEOUT 8u      /* a bounded on-chip wait gave up; outputs of that launch are invalid */
 
 /* ABI version of this header (bumped on any incompatible change). */
 #define CSA2_ABI_VERSION 1

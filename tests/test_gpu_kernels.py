@@ -45,8 +45,15 @@ def test_pack_mxfp4_bit_exact():
     scales = torch.empty(x.shape[0], 32, dtype=torch.uint8, device="cuda")
     abi.csa2_pack_mxfp4_f32(x.cuda(), codes, scales)
     rc, rs = F.mxfp4_pack(x.numpy())
-    assert np.array_equal(scales.cpu().numpy(), rs)
-    assert np.array_equal(codes.cpu().numpy(), rc)
+    gs, gc = scales.cpu().numpy(), codes.cpu().numpy()
+    assert np.array_equal(gs, rs)
+    bad = np.argwhere(gc != rc)
+    if len(bad):
+        r, byte = bad[0]
+        grp = byte // 8
+        xs = x[r, grp * 16:(grp + 1) * 16].numpy()
+        raise AssertionError(f"{len(bad)} code bytes differ; first at row {r} byte {byte}: gpu {gc[r, byte]:#04x} "
+                             f"oracle {rc[r, byte]:#04x}; scale {rs[r, grp]:#04x}; group {xs.tolist()}")
 
 
 def test_pack_mxfp4_d64_and_ragged_rows():
@@ -92,8 +99,11 @@ def _score_rows():
     g = torch.Generator().manual_seed(15)
     rows, n_valid = [], []
     stride = 40000
+    # "const" and "narrow" put more than 4,096 entries in the threshold bin of the
+    # 11-bit key histogram, which takes the whole-row radix path
     for n, kind in [(40000, "normal"), (33333, "ties"), (5000, "ties2"), (512, "normal"), (300, "normal"),
-                    (0, "normal"), (1, "normal"), (513, "zeros"), (20000, "neg"), (16385, "ties")]:
+                    (0, "normal"), (1, "normal"), (513, "zeros"), (20000, "neg"), (16385, "ties"),
+                    (40000, "const"), (30000, "narrow")]:
         if kind == "normal":
             r = torch.randn(stride, generator=g)
         elif kind == "ties":
@@ -104,6 +114,10 @@ def _score_rows():
             r = torch.zeros(stride)
             r[torch.randperm(stride, generator=g)[:200]] = -0.0
             r[5] = 1.0
+        elif kind == "const":
+            r = torch.full((stride,), 2.5)
+        elif kind == "narrow":
+            r = 1.0 + torch.rand(stride, generator=g) * 0.2
         else:
             r = -torch.rand(stride, generator=g) * 1e-30 - 1e-38
         r[n:] = float("nan")   # never read: beyond the valid count
