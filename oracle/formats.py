@@ -58,7 +58,12 @@ _E4M3_POS = [(c, E4M3_TABLE[c]) for c in range(128) if not np.isnan(E4M3_TABLE[c
 
 
 def _nearest_even_code(mag: float, candidates) -> int:
-    """Code of the candidate nearest to mag; ties go to the even code."""
+    """Code of the candidate nearest to mag; ties go to the even code.
+
+    Magnitudes beyond the largest finite value saturate to it (satfinite):
+    the clamp comes first, so the distances stay exact for huge inputs.
+    """
+    mag = min(mag, max(v for _, v in candidates))
     best_code, best_dist = None, None
     for c, v in candidates:
         dist = abs(v - mag)
@@ -85,7 +90,8 @@ def e4m3_encode(x: float) -> int:
 
 def _encode_array(x: np.ndarray, candidates, sign_bit: int) -> np.ndarray:
     x = np.asarray(x, dtype=np.float32).astype(np.float64)
-    mag = np.abs(x)
+    # satfinite: clamp to the largest finite magnitude before measuring distances
+    mag = np.minimum(np.abs(x), max(v for _, v in candidates))
     best = np.zeros(x.shape, dtype=np.int64)
     best_d = np.full(x.shape, np.inf)
     for c, v in candidates:

@@ -55,6 +55,9 @@ def test_e4m3_encoder_matches_torch_cast():
 def test_e4m3_saturates():
     assert F.e4m3_encode(500.0) == 0x7E
     assert F.e4m3_encode(-1e30) == 0xFE
+    assert F.e4m3_encode(3e38) == 0x7E
+    assert np.array_equal(F.e4m3_encode_array(np.array([1e38, -2e37], np.float32)), [0x7E, 0xFE])
+    assert np.array_equal(F.e2m1_encode_array(np.array([1e38, -2e37], np.float32)), [0x7, 0xF])
     assert F.e4m3_encode(0.0) == 0x00
     assert F.e4m3_encode(-0.0) == 0x80
 
@@ -63,6 +66,7 @@ def test_e4m3_saturates():
     (0.25, 0x0), (0.26, 0x1), (0.75, 0x2), (1.25, 0x2), (1.26, 0x3), (1.75, 0x4),
     (2.5, 0x4), (2.6, 0x5), (3.5, 0x6), (5.0, 0x6), (5.1, 0x7), (7.0, 0x7), (1e9, 0x7),
     (-0.1, 0x8), (-1.75, 0xC), (-6.0, 0xF), (0.5, 0x1), (3.0, 0x5),
+    (2.2e35, 0x7), (-3e38, 0xF),
 ])
 def test_e2m1_round_to_nearest_even(x, code):
     assert F.e2m1_encode(x) == code
