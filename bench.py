@@ -254,7 +254,7 @@ def time_dominant_kernel(args, g, wl, flush, stream):
         stride = g.max_entries
         scores = torch.empty(wl.B * wl.Tq, stride, dtype=torch.float32, device=flush.device)
         fn = lambda: abi.csa2_index_scores(g.dims(), g.cache(), g.idx_q[0], g.idx_w[0], g.q_pos, scores)  # noqa
-        name = "k_index_scores_mma"
+        name = "k_index_scan_pages"
     else:              # prefill: attention of the Full layer
         fn = lambda: abi.csa2_sparse_attn(g.dims(), g.cache(), g.window(0), g.Q[0], g.q_pos, g.idx[0],  # noqa
                                           g.cnt[0], 1.0 / math.sqrt(wl.d), g.O[0], g.lse[0])
@@ -317,7 +317,7 @@ def load_peaks():
 
 def roofline(wl, alg, kern, peaks):
     src = os.path.join(ROOT, "compressed_sparse_attention_05_gb300", "csrc")
-    if kern["name"] == "k_index_scores_mma":
+    if kern["name"] == "k_index_scan_pages":
         bytes_ = alg["scan_bytes"]
         achieved = bytes_ / (kern["ms"] / 1e3) / 1e9
         traffic = committed_traffic(os.path.join(ROOT, "profiles", f"index_scores_{wl.name}.md"),

@@ -263,7 +263,7 @@ k_compress_gemm_tc(const uint16_t* __restrict__ hidden, int G, int T, int H, con
 
 // The tensor-memory GEMM is used once its operand layout has been checked on
 // the GPU; the mma.sync kernel stays for shapes it does not take.
-constexpr bool kUseTcCompress = false;
+constexpr bool kUseTcCompress = true;
 
 static int compress_splits(int M, int N, int Kd) {
   const int tiles = ((M + kGM - 1) / kGM) * ((N + kGN - 1) / kGN);

@@ -13,6 +13,7 @@
 // makes every warp load instruction touch 16 full 32-byte sectors.
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 namespace csa2 {
 
@@ -183,6 +184,190 @@ k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t st
   }
 }
 
+// ---- page-streaming scan (Full mode, bf16 keys, Di = 128) ---------------------------
+// One lane of a producer warp streams whole key pages (64 entries x 256 B =
+// 16 KB, contiguous in the pool) into a ring of shared-memory stages with
+// cp.async.bulk; each stage completes on an mbarrier with its byte count.
+// Four consumer warps take 16 entries each per page and run the same tensor-
+// core scoring as above from shared memory, then release the stage.  Many
+// pages per SM stay in flight, which is what an HBM-bound scan needs.
+// Every wait is bounded; on a timeout the CTA raises CSA2_STATUS_TIMEOUT,
+// drains the copies it issued and exits.
+constexpr int kScanStages = 6;
+constexpr int kScanConsumers = 4;
+constexpr int kScanThreads = (kScanConsumers + 1) * 32;
+constexpr int kPageBytes = kPage * 128 * 2;
+
+struct ScanShared {
+  uint64_t full[kScanStages];
+  uint64_t empty[kScanStages];
+  int valid[kScanStages];
+  int abort;
+};
+
+// Waits for `parity` on `bar` while no other role has aborted.
+__device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kScanThreads)
+k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, float* __restrict__ scores, int64_t stride,
+                   float* __restrict__ blockmax, int64_t bm_stride, uint32_t* __restrict__ hist,
+                   uint32_t* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  __shared__ ScanShared ss;
+  unsigned char* ring = smem_raw;                                   // kScanStages pages
+  uint32_t* shist = reinterpret_cast<uint32_t*>(smem_raw + kScanStages * kPageBytes);
+  const int b = blockIdx.z;
+  const int i0 = blockIdx.y * QG;
+  const int i1 = min(a.Tq, i0 + QG);
+  const int n_ent = min(a.n_entries[b], a.max_entries);
+  int max_vis = 0;
+  for (int i = i0; i < i1; ++i) max_vis = max(max_vis, n_visible(n_ent, a.q_pos[(int64_t)b * a.Tq + i]));
+  const int p0 = blockIdx.x * pages_per_cta;
+  const int p1 = min((max_vis + kPage - 1) / kPage, p0 + pages_per_cta);
+  if (p0 >= p1) return;
+  const int n_pages = p1 - p0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      tc::mbar_init(&ss.full[s], 1);
+      tc::mbar_init(&ss.empty[s], kScanConsumers);
+    }
+    ss.abort = 0;
+    tc::mbar_fence_init();
+  }
+  if (hist)
+    for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) shist[i] = 0;
+  __syncthreads();
+  volatile int* abort = &ss.abort;
+
+  if (warp == kScanConsumers) {
+    // ---- producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < n_pages; ++i) {
+        const int st = i % kScanStages;
+        if (i >= kScanStages && !scan_wait(&ss.empty[st], ((i / kScanStages) - 1) & 1, abort)) break;
+        const int lp = p0 + i;
+        const int pg = lp < a.max_pages ? a.page_table[(int64_t)b * a.max_pages + lp] : -1;
+        if (pg < 0 || pg >= a.n_pages) {
+          raise_status(status, CSA2_STATUS_BAD_PAGE);
+          ss.valid[st] = 0;
+          tc::mbar_arrive(&ss.full[st]);
+        } else {
+          ss.valid[st] = 1;
+          tc::mbar_arrive_expect_tx(&ss.full[st], kPageBytes);
+          tc::bulk_g2s(ring + st * kPageBytes,
+                       reinterpret_cast<const unsigned char*>(a.k) + (int64_t)pg * kPageBytes, kPageBytes,
+                       &ss.full[st]);
+        }
+        issued = i + 1;
+      }
+      // drain: every issued copy must have landed before the CTA exits
+      for (int i = max(0, issued - kScanStages); i < issued; ++i) {
+        const int st = i % kScanStages;
+        for (uint32_t k = 0; k < (1u << 22); ++k)
+          if (tc::mbar_try_wait(&ss.full[st], (i / kScanStages) & 1)) break;
+      }
+    }
+  } else {
+    // ---- consumers: warp w owns entries 16w .. 16w+15 of every page
+    const int g = lane >> 2, t = lane & 3;
+    for (int i = 0; i < n_pages; ++i) {
+      const int st = i % kScanStages;
+      if (!scan_wait(&ss.full[st], (i / kScanStages) & 1, abort)) break;
+      if (ss.valid[st]) {
+        const unsigned char* pg = ring + st * kPageBytes + (warp * 16) * 256 + 16 * t;
+        uint4 ka[4], kb[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          ka[c] = *reinterpret_cast<const uint4*>(pg + g * 256 + 64 * c);
+          kb[c] = *reinterpret_cast<const uint4*>(pg + (g + 8) * 256 + 64 * c);
+        }
+        const int e0 = (p0 + i) * kPage + warp * 16;
+        for (int qi = i0; qi < i1; ++qi) {
+          const int64_t row = (int64_t)b * a.Tq + qi;
+          const int nv = n_visible(n_ent, a.q_pos[row]);
+          if (e0 >= nv) continue;
+          uint4 qf[NT][4];
+          float wv[NT][2];
+          load_query<4, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi, a.Hi,
+                            a.Di, lane, qf, wv);
+          float sg, sg8;
+          tile_scores<4, NT>(ka, kb, qf, wv, sg, sg8);
+          const bool vg = e0 + g < nv, vg8 = e0 + g + 8 < nv;
+          if (t == 0 && vg) scores[row * stride + e0 + g] = sg;
+          if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
+          if (hist) {
+            const bool has = (t == 0 && vg) || (t == 1 && vg8);
+            const uint32_t bin = has ? score_key(t == 0 ? sg : sg8) >> 21 : 0xFFFFFFFFu;
+            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+            if (has && lane == __ffs(peers) - 1) atomicAdd(&shist[(qi - i0) * kHistBins + bin], __popc(peers));
+          }
+          if (blockmax) {
+            float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+              m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (lane == 0) blockmax[row * bm_stride + e0 / 8] = m0;
+            if (lane == 1 && e0 + 8 < nv) blockmax[row * bm_stride + e0 / 8 + 1] = m1;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&ss.empty[st]);
+    }
+  }
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) raise_status(status, CSA2_STATUS_TIMEOUT);
+  if (hist) {
+    for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) {
+      const uint32_t c = shist[i];
+      if (c) atomicAdd(&hist[((int64_t)b * a.Tq + i0 + i / kHistBins) * kHistBins + (i % kHistBins)], c);
+    }
+  }
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int NT>
+static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
+                                     int64_t bm_stride, int max_entries, uint32_t* hist, cudaStream_t s) {
+  const int QG = a.Tq >= kHistMaxQG ? kHistMaxQG : a.Tq;
+  const int q_groups = (a.Tq + QG - 1) / QG;
+  const int max_pages_vis = (max_entries + kPage - 1) / kPage;
+  // about two CTAs per SM over the whole grid
+  const int64_t want = 2LL * num_sms();
+  int per_seq = (int)((want + (int64_t)a.B * q_groups - 1) / ((int64_t)a.B * q_groups));
+  per_seq = per_seq < 1 ? 1 : per_seq;
+  int ppc = (max_pages_vis + per_seq - 1) / per_seq;
+  ppc = ppc < 1 ? 1 : ppc;
+  const size_t smem = (size_t)kScanStages * kPageBytes + (hist ? (size_t)QG * kHistBins * 4 : 0);
+  cudaError_t e = cudaFuncSetAttribute(k_index_scan_pages<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((max_pages_vis + ppc - 1) / ppc, q_groups, a.B);
+  k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, QG, ppc, scores, stride, blockmax, bm_stride, hist,
+                                                          status_word());
+  return counted(cudaGetLastError());
+}
+
 // Histogram of already-written scores (the generic scoring path).
 __global__ void k_score_hist(const float* __restrict__ scores, int64_t stride, IndexerArgs a,
                              uint32_t* __restrict__ hist) {
@@ -345,6 +530,10 @@ static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, co
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
                                 int64_t bm_stride, int block, int max_entries, uint32_t* hist, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0 || max_entries == 0) return cudaSuccess;
+  if (mma_path(a) && block == 8 && a.Di == 128) {
+    if (a.Hi > 8) return launch_scan_pages<2>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
+    return launch_scan_pages<1>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
+  }
   if (mma_path(a) && block == 8) {
     CSA2_DISPATCH_MMA(launch_full_mma, a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
   }

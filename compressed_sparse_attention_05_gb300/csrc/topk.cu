@@ -23,7 +23,6 @@ namespace csa2 {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 4096;      // candidates of the threshold bin kept in smem
-constexpr int kSelCap = 4096;       // largest K
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -127,30 +126,18 @@ __device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int ne
   return s_digit;
 }
 
-// Ascending bitonic sort of n2 (a power of two) 32-bit values in shared memory.
-template <typename T>
-__device__ __forceinline__ void block_bitonic_sort(T* a, int n2) {
-  for (int kb = 2; kb <= n2; kb <<= 1)
-    for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-      for (int i = threadIdx.x; i < n2; i += kTopkThreads) {
-        const int ixj = i ^ jb;
-        if (ixj > i) {
-          const T x = a[i], y = a[ixj];
-          if ((x > y) == ((i & kb) == 0)) { a[i] = y; a[ixj] = x; }
-        }
-      }
-      __syncthreads();
-    }
-}
+constexpr int kBitmapMax = 1 << 18;            // rows up to 262,144 entries use bitmaps
+constexpr int kBitmapWords = kBitmapMax / 32;
 
 struct TopkSmem {
   uint32_t hist[2048];
   uint32_t hist2[256];
   int warp_tot[kTopkWarps];
-  int nA, nC, nT;
-  int32_t sel[kSelCap];           // selected indices (unsorted), then sorted
+  int nC;
   uint32_t ckey[kCandCap];        // candidate keys of the threshold bin
   int32_t cidx[kCandCap];         // and their indices
+  uint32_t sel_bits[kBitmapWords];  // selected entries, one bit per index
+  uint32_t tie_bits[kBitmapWords];  // entries equal to the K-th key
 };
 
 __global__ void __launch_bounds__(kTopkThreads)
@@ -163,7 +150,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
   const int n = row_valid(v, row, stride);
   const int kk = min(k, n);
   int32_t* out = out_idx + row * (int64_t)k;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
 
   for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
   if (tid == 0) out_cnt[row] = kk;
@@ -184,15 +171,18 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
       warp_hist_add(sm.hist, j < n ? order_key(s[j]) >> 21 : 0xFFFFFFFFu, 2048);
     }
   }
-  if (tid == 0) { sm.nA = 0; sm.nC = 0; sm.nT = 0; }
+  if (tid == 0) sm.nC = 0;
   __syncthreads();
   int above;
   const int bstar = find_digit(sm.hist, 2048, kk, sm.warp_tot, &above);
   int need = kk - above;                  // entries of bin bstar to take
   const int n_bin = (int)sm.hist[bstar];
 
-  if (n_bin <= kCandCap) {
-    // ---- one pass: higher bins -> selected; bin bstar -> candidates
+  if (n_bin <= kCandCap && n <= kBitmapMax) {
+    const int words = (n + 31) / 32;
+    for (int i = tid; i < words; i += kTopkThreads) sm.tie_bits[i] = 0;
+    // ---- one pass: higher bins -> selection bitmap; bin bstar -> candidate list
+    // (lanes of a warp cover one aligned 32-entry word, so the ballot is the word)
     for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
       const int j = j0 + tid;
       uint32_t key = 0, bin = 0;
@@ -200,8 +190,8 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
         key = order_key(s[j]);
         bin = key >> 21;
       }
-      const int ps = warp_slot(&sm.nA, j < n && bin > (uint32_t)bstar, kSelCap);
-      if (ps >= 0) sm.sel[ps] = j;
+      const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
+      if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
       const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
       if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
     }
@@ -230,38 +220,41 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
       prefix |= (uint32_t)dg << sh;
       mask |= (nb - 1) << sh;
     }
-    const uint32_t T = prefix;             // exact K-th key; `need` ties at T are taken
-    // candidates above T join the selection; indices of ties at T go to cidx[0..nT)
-    // (written only after every thread has read its candidate of the round)
-    for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      const bool ok = i < nC;
-      const uint32_t key = ok ? sm.ckey[i] : 0;
-      const int32_t idx = ok ? sm.cidx[i] : 0;
-      __syncthreads();
-      const int ps = warp_slot(&sm.nA, ok && key > T, kSelCap);
-      if (ps >= 0) sm.sel[ps] = idx;
-      const int pt = warp_slot(&sm.nT, ok && key == T, kCandCap);
-      if (pt >= 0) sm.cidx[pt] = idx;
-      __syncthreads();
+    const uint32_t T = prefix;             // exact K-th key; `need` entries equal to T are taken
+    for (int i = tid; i < nC; i += kTopkThreads) {
+      const uint32_t key = sm.ckey[i];
+      const int32_t j = sm.cidx[i];
+      if (key > T) atomicOr(&sm.sel_bits[j >> 5], 1u << (j & 31));
+      else if (key == T) atomicOr(&sm.tie_bits[j >> 5], 1u << (j & 31));
     }
-    const int nT = min(sm.nT, kCandCap);
-    // ties: the `need` lowest indices
-    int nt2 = 1;
-    while (nt2 < nT) nt2 <<= 1;
-    for (int i = nT + tid; i < nt2; i += kTopkThreads) sm.cidx[i] = 0x7FFFFFFF;
     __syncthreads();
-    block_bitonic_sort(sm.cidx, nt2);
-    const int base = min(sm.nA, kSelCap);
-    for (int i = tid; i < need && i < nT && base + i < kSelCap; i += kTopkThreads) sm.sel[base + i] = sm.cidx[i];
-    __syncthreads();
-    // sort the kk selected indices ascending and write them
-    int n2 = 1;
-    while (n2 < kk) n2 <<= 1;
-    for (int i = kk + tid; i < n2; i += kTopkThreads) sm.sel[i] = 0x7FFFFFFF;
-    __syncthreads();
-    block_bitonic_sort(sm.sel, n2);
-    for (int i = tid; i < kk; i += kTopkThreads) out[i] = remap_index(remap, row, sm.sel[i]);
+    // ---- index-ordered output: thread tid owns words [w0, w1)
+    const int per = (words + kTopkThreads - 1) / kTopkThreads;
+    const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+    int ties = 0;
+    for (int w = w0; w < w1; ++w) ties += __popc(sm.tie_bits[w]);
+    int ties_before = block_exclusive_scan(ties, sm.warp_tot);
+    int cnt = 0;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t tb = sm.tie_bits[w];
+      while (tb && ties_before < need) {      // lowest indices first
+        const uint32_t low = tb & (0u - tb);
+        sm.sel_bits[w] |= low;
+        tb ^= low;
+        ++ties_before;
+      }
+      cnt += __popc(sm.sel_bits[w]);
+    }
+    int pos = block_exclusive_scan(cnt, sm.warp_tot);
+    for (int w = w0; w < w1; ++w) {
+      uint32_t sb = sm.sel_bits[w];
+      while (sb) {
+        const int bit = __ffs(sb) - 1;
+        sb &= sb - 1;
+        if (pos < kk) out[pos] = remap_index(remap, row, w * 32 + bit);
+        ++pos;
+      }
+    }
     return;
   }
 
