@@ -215,24 +215,63 @@ __device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
+// Pages of a single-query row b: ceil(visible / 64).
+__device__ __forceinline__ int row_pages(const IndexerArgs& a, int b) {
+  const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[(int64_t)b * a.Tq]);
+  return (nv + kPage - 1) / kPage;
+}
+
+// Balanced single-wave partition when every row has one query (Tq == 1):
+// with P pages in all and S CTA slots, every row gets ceil(pages_b / ppc)
+// CTAs of ppc = ceil(P / (S - B)) pages, so the grid never exceeds S and no
+// CTA spans two rows.  Each CTA derives its (row, page range) itself.
+__device__ __forceinline__ bool flat_assign(const IndexerArgs& a, int slots, int& b_out, int& p0, int& p1) {
+  int64_t total = 0;
+  for (int b = 0; b < a.B; ++b) total += row_pages(a, b);
+  const int denom = max(1, slots - a.B);
+  int64_t ppc64 = (total + denom - 1) / denom;
+  const int ppc = ppc64 < 1 ? 1 : (int)ppc64;
+  int c = blockIdx.x;
+  for (int b = 0; b < a.B; ++b) {
+    const int pb = row_pages(a, b);
+    const int nc = (pb + ppc - 1) / ppc;
+    if (c < nc) {
+      b_out = b;
+      p0 = c * ppc;
+      p1 = min(pb, p0 + ppc);
+      return p0 < p1;
+    }
+    c -= nc;
+  }
+  return false;
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kScanThreads)
-k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, float* __restrict__ scores, int64_t stride,
-                   float* __restrict__ blockmax, int64_t bm_stride, uint32_t* __restrict__ hist,
+k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, float* __restrict__ scores,
+                   int64_t stride, float* __restrict__ blockmax, int64_t bm_stride, uint32_t* __restrict__ hist,
                    uint32_t* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ ScanShared ss;
   unsigned char* ring = smem_raw;                                   // kScanStages pages
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem_raw + kScanStages * kPageBytes);
-  const int b = blockIdx.z;
-  const int i0 = blockIdx.y * QG;
-  const int i1 = min(a.Tq, i0 + QG);
+  int b, p0, p1, i0, i1;
+  if (flat_slots > 0) {          // one query per row
+    if (!flat_assign(a, flat_slots, b, p0, p1)) return;
+    i0 = 0;
+    i1 = 1;
+  } else {
+    b = blockIdx.z;
+    i0 = blockIdx.y * QG;
+    i1 = min(a.Tq, i0 + QG);
+    const int n_ent_b = min(a.n_entries[b], a.max_entries);
+    int max_vis = 0;
+    for (int i = i0; i < i1; ++i) max_vis = max(max_vis, n_visible(n_ent_b, a.q_pos[(int64_t)b * a.Tq + i]));
+    p0 = blockIdx.x * pages_per_cta;
+    p1 = min((max_vis + kPage - 1) / kPage, p0 + pages_per_cta);
+    if (p0 >= p1) return;
+  }
   const int n_ent = min(a.n_entries[b], a.max_entries);
-  int max_vis = 0;
-  for (int i = i0; i < i1; ++i) max_vis = max(max_vis, n_visible(n_ent, a.q_pos[(int64_t)b * a.Tq + i]));
-  const int p0 = blockIdx.x * pages_per_cta;
-  const int p1 = min((max_vis + kPage - 1) / kPage, p0 + pages_per_cta);
-  if (p0 >= p1) return;
   const int n_pages = p1 - p0;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -280,9 +319,17 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, float* __restrict__
   } else {
     // ---- consumers: warp w owns entries 16w .. 16w+15 of every page
     const int g = lane >> 2, t = lane & 3;
+    uint4 qf1[NT][4];      // the query of a single-query CTA, loaded once
+    float wv1[NT][2];
+    if (i1 - i0 == 1) {
+      const int64_t row = (int64_t)b * a.Tq + i0;
+      load_query<4, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi, a.Hi, a.Di,
+                        lane, qf1, wv1);
+    }
     for (int i = 0; i < n_pages; ++i) {
       const int st = i % kScanStages;
-      if (!scan_wait(&ss.full[st], (i / kScanStages) & 1, abort)) break;
+      // warp-uniform exit: the warp's shuffles below need every lane
+      if (!__all_sync(0xffffffffu, scan_wait(&ss.full[st], (i / kScanStages) & 1, abort))) break;
       if (ss.valid[st]) {
         const unsigned char* pg = ring + st * kPageBytes + (warp * 16) * 256 + 16 * t;
         uint4 ka[4], kb[4];
@@ -296,12 +343,16 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, float* __restrict__
           const int64_t row = (int64_t)b * a.Tq + qi;
           const int nv = n_visible(n_ent, a.q_pos[row]);
           if (e0 >= nv) continue;
-          uint4 qf[NT][4];
-          float wv[NT][2];
-          load_query<4, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi, a.Hi,
-                            a.Di, lane, qf, wv);
           float sg, sg8;
-          tile_scores<4, NT>(ka, kb, qf, wv, sg, sg8);
+          if (i1 - i0 == 1) {
+            tile_scores<4, NT>(ka, kb, qf1, wv1, sg, sg8);
+          } else {
+            uint4 qf[NT][4];
+            float wv[NT][2];
+            load_query<4, NT>(reinterpret_cast<const uint16_t*>(a.q) + row * a.Hi * a.Di, a.w + row * a.Hi, a.Hi,
+                              a.Di, lane, qf, wv);
+            tile_scores<4, NT>(ka, kb, qf, wv, sg, sg8);
+          }
           const bool vg = e0 + g < nv, vg8 = e0 + g + 8 < nv;
           if (t == 0 && vg) scores[row * stride + e0 + g] = sg;
           if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
@@ -362,8 +413,19 @@ static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_
   const size_t smem = (size_t)kScanStages * kPageBytes + (hist ? (size_t)QG * kHistBins * 4 : 0);
   cudaError_t e = cudaFuncSetAttribute(k_index_scan_pages<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (a.Tq == 1) {
+    // CTA slots resident at once (shared memory bounds the CTAs per SM)
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_index_scan_pages<NT>, kScanThreads, smem);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+    const int slots = per_sm * num_sms();
+    const int grid = slots > a.B ? slots : a.B + 1;
+    k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, 1, 0, grid, scores, stride, blockmax, bm_stride,
+                                                             hist, status_word());
+    return counted(cudaGetLastError());
+  }
   dim3 grid((max_pages_vis + ppc - 1) / ppc, q_groups, a.B);
-  k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, QG, ppc, scores, stride, blockmax, bm_stride, hist,
+  k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, QG, ppc, 0, scores, stride, blockmax, bm_stride, hist,
                                                           status_word());
   return counted(cudaGetLastError());
 }

@@ -23,6 +23,7 @@ namespace csa2 {
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCandCap = 4096;      // candidates of the threshold bin kept in smem
+constexpr int kBatch = 8;           // row elements loaded per thread before they are used
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -166,9 +167,18 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
   } else {
     for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
     __syncthreads();
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
-      const int j = j0 + tid;
-      warp_hist_add(sm.hist, j < n ? order_key(s[j]) >> 21 : 0xFFFFFFFFu, 2048);
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {   // independent loads first
+        const int j = j0 + u * kTopkThreads + tid;
+        v[u] = j < n ? s[j] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        warp_hist_add(sm.hist, j < n ? order_key(v[u]) >> 21 : 0xFFFFFFFFu, 2048);
+      }
     }
   }
   if (tid == 0) sm.nC = 0;
@@ -183,17 +193,26 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
     for (int i = tid; i < words; i += kTopkThreads) sm.tie_bits[i] = 0;
     // ---- one pass: higher bins -> selection bitmap; bin bstar -> candidate list
     // (lanes of a warp cover one aligned 32-entry word, so the ballot is the word)
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
-      const int j = j0 + tid;
-      uint32_t key = 0, bin = 0;
-      if (j < n) {
-        key = order_key(s[j]);
-        bin = key >> 21;
+    for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {   // independent loads first
+        const int j = j0 + u * kTopkThreads + tid;
+        v[u] = j < n ? s[j] : 0.f;
       }
-      const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
-      if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
-      const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
-      if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        uint32_t key = 0, bin = 0;
+        if (j < n) {
+          key = order_key(v[u]);
+          bin = key >> 21;
+        }
+        const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
+        if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
+        const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
+        if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
+      }
     }
     __syncthreads();
     const int nC = min(sm.nC, kCandCap);
