@@ -311,6 +311,8 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
 constexpr int kPipeConsumers = 8;
 constexpr int kPipeThreads = (kPipeConsumers + 1) * 32;
 constexpr int kStageCodes = 512;  // bytes per key of staged codes (window rows need d bytes)
+constexpr int kStages = 3;        // staging depth (tiles in flight ahead of the consumers)
+constexpr int kMaxKeys = 2048 + 1024;  // K + W upper bound: key sources resolved up front
 
 struct PipeSmem {
   static constexpr int QS = 512 + 8, PS = kTK + 8;
@@ -318,11 +320,11 @@ struct PipeSmem {
   uint16_t k[kTK * QS];
   float s[kHG * kTK];
   uint16_t p[kHG * PS];
-  uint8_t codes[2][kTK][kStageCodes];
-  uint8_t scales[2][kTK][32];
-  float wscale[2][kTK];
-  int64_t key_src[2][kTK];
-  uint64_t full[2], empty[2];
+  uint8_t codes[kStages][kTK][kStageCodes];
+  uint8_t scales[kStages][kTK][32];
+  float wscale[kStages][kTK];
+  int64_t key_src[kStages][kTK];
+  uint64_t full[kStages], empty[kStages];
   float m[kHG], l[kHG], alpha[kHG];
   int abort;
 };
@@ -378,7 +380,7 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
   const int n_tiles = (n_keys + kTK - 1) / kTK;
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       tc::mbar_init(&sm.full[i], 1);
       tc::mbar_init(&sm.empty[i], 1);
     }
@@ -389,6 +391,20 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
     sm.m[tid] = -INFINITY;
     sm.l[tid] = 0.f;
   }
+  // resolve every key's source once, with all threads: index -> page table ->
+  // pool slot for selected entries, window row for the rest (-1 = no key)
+  int64_t* slots = reinterpret_cast<int64_t*>(smem_raw + sizeof(PipeSmem));
+  for (int i = tid; i < n_keys; i += kPipeThreads) {
+    int64_t sv = -1;
+    if (i < n_sel) {
+      const int j = a.idx[row * a.K + i];
+      if (j >= 0 && j < nv) sv = entry_slot(a.page_table, a.max_pages, a.n_pages, b, j, status);
+      else raise_status(status, CSA2_STATUS_BAD_INDEX);
+    } else {
+      sv = -2 - (int64_t)(w_lo + (i - n_sel) - pos0);
+    }
+    slots[i] = sv;
+  }
   __syncthreads();
   volatile int* abort = &sm.abort;
 
@@ -396,10 +412,10 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
     // ---------------- producer
     int issued = 0;
     for (int ti = 0; ti < n_tiles; ++ti) {
-      const int st = ti & 1;
+      const int st = ti % kStages;
       // lane 0 waits for the stage; the warp follows its answer (warp-uniform exit)
       bool okw = true;
-      if (ti >= 2 && lane == 0) okw = pipe_wait(&sm.empty[st], ((ti >> 1) - 1) & 1, abort);
+      if (ti >= kStages && lane == 0) okw = pipe_wait(&sm.empty[st], ((ti / kStages) - 1) & 1, abort);
       if (!__shfl_sync(0xffffffffu, okw, 0)) break;
       int64_t src[2];
       uint32_t bytes = 0;
@@ -407,16 +423,11 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
       for (int h = 0; h < 2; ++h) {
         const int kr = lane * 2 + h;
         const int i = ti * kTK + kr;
-        int64_t sv = -1;
-        if (i < n_sel) {
-          const int j = a.idx[row * a.K + i];
-          if (j >= 0 && j < nv) sv = entry_slot(a.page_table, a.max_pages, a.n_pages, b, j, status);
-          else raise_status(status, CSA2_STATUS_BAD_INDEX);
-          if (sv >= 0) bytes += 256 + 32;
-        } else if (i < n_keys) {
-          const int64_t wr = w_lo + (i - n_sel) - pos0;
-          sv = -2 - wr;
-          sm.wscale[st][kr] = a.swa_scales[(int64_t)b * a.swa_cap + wr];
+        const int64_t sv = i < n_keys ? slots[i] : -1;
+        if (sv >= 0) {
+          bytes += 256 + 32;
+        } else if (sv <= -2) {
+          sm.wscale[st][kr] = a.swa_scales[(int64_t)b * a.swa_cap + (-2 - sv)];
           bytes += D;
         }
         src[h] = sv;
@@ -441,9 +452,9 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
     }
     // drain the copies still in flight before the CTA can exit
     if (lane == 0)
-      for (int ti = max(0, issued - 2); ti < issued; ++ti)
+      for (int ti = max(0, issued - kStages); ti < issued; ++ti)
         for (uint32_t k2 = 0; k2 < (1u << 22); ++k2)
-          if (tc::mbar_try_wait(&sm.full[ti & 1], (ti >> 1) & 1)) break;
+          if (tc::mbar_try_wait(&sm.full[ti % kStages], (ti / kStages) & 1)) break;
   } else {
     // ---------------- consumers
     const int g = lane >> 2, t4 = lane & 3;
@@ -469,8 +480,8 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
     const float sl2 = a.scale * 1.4426950408889634f;
 
     for (int ti = 0; ti < n_tiles; ++ti) {
-      const int st = ti & 1;
-      if (!consumer_vote_and(pipe_wait(&sm.full[st], (ti >> 1) & 1, abort))) break;
+      const int st = ti % kStages;
+      if (!consumer_vote_and(pipe_wait(&sm.full[st], (ti / kStages) & 1, abort))) break;
       // ---- dequantise the staged tile: item = (key, 16-channel group)
       for (int it = tid; it < kTK * (D / 16); it += kPipeConsumers * 32) {
         const int kr = it & (kTK - 1), grp = it / kTK;
@@ -505,20 +516,27 @@ k_sparse_attn_pipe(AttnArgs a, uint32_t* status) {
         d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
       consumer_sync();
-      // ---- S = Q K^T : warp owns keys 8*warp .. +7
+      // ---- S = Q K^T : warp owns keys 8*warp .. +7; four independent
+      // accumulators keep the tensor-core dependency chain short
       {
-        float s0[4] = {0.f, 0.f, 0.f, 0.f};
+        float sa[4][4] = {};
         const uint32_t qa = smem_u32(&sm.q[(lane & 15) * QS + (lane >> 4) * 8]);
         const uint32_t kb = smem_u32(&sm.k[(warp * 8 + (lane & 7)) * QS + (lane >> 3) * 8]);
-#pragma unroll 4
-        for (int ks = 0; ks < D / 32; ++ks) {
-          uint32_t a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3;
-          ldsm_x4(qa + ks * 64, a0, a1, a2, a3);
-          ldsm_x4(qa + ks * 64 + 32, a4, a5, a6, a7);
-          ldsm_x4(kb + ks * 64, b0, b1, b2, b3);
-          mma_f16(s0, a0, a1, a2, a3, b0, b1);
-          mma_f16(s0, a4, a5, a6, a7, b2, b3);
+#pragma unroll
+        for (int ks = 0; ks < D / 32; ks += 2) {
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            uint32_t a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3;
+            ldsm_x4(qa + (ks + u) * 64, a0, a1, a2, a3);
+            ldsm_x4(qa + (ks + u) * 64 + 32, a4, a5, a6, a7);
+            ldsm_x4(kb + (ks + u) * 64, b0, b1, b2, b3);
+            mma_f16(sa[2 * u], a0, a1, a2, a3, b0, b1);
+            mma_f16(sa[2 * u + 1], a4, a5, a6, a7, b2, b3);
+          }
         }
+        float s0[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) s0[r] = (sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r]);
         const int key0 = warp * 8 + 2 * t4;
         const bool v0 = sm.key_src[st][key0] != -1, v1 = sm.key_src[st][key0 + 1] != -1;
         sm.s[g * kTK + key0] = v0 ? s0[0] * sl2 : -INFINITY;
@@ -617,8 +635,8 @@ static cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s) {
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0) return cudaSuccess;
-  if (a.d == 512) {
-    const size_t smem = sizeof(PipeSmem);
+  if (a.d == 512 && a.K + a.W <= kMaxKeys) {
+    const size_t smem = sizeof(PipeSmem) + (size_t)(a.K + a.W) * sizeof(int64_t);
     cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_pipe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Hq + kHG - 1) / kHG, (unsigned)((int64_t)a.B * a.Tq));
