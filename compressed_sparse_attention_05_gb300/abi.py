@@ -82,6 +82,9 @@ SIGNATURES = {
     "csa2_index_topk_workspace_size": (_SZ, [C.POINTER(Dims), _I32]),
     "csa2_index_topk": (C.c_int, [C.POINTER(Dims), C.POINTER(Cache), _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _I32, _P, _SZ, _P]),
+    "csa2_index_topk_noalloc_capacity": (_SZ, []),
+    "csa2_index_topk_noalloc": (C.c_int, [C.POINTER(Dims), C.POINTER(Cache), _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                          _I32, _P]),
     "csa2_sparse_attn": (C.c_int, [C.POINTER(Dims), C.POINTER(Cache), C.POINTER(Window), _P, _P, _P, _P,
                                    _F, _P, _P, _P]),
     "csa2_layer_workspace_size": (_SZ, [C.POINTER(LayerArgs)]),
@@ -219,6 +222,18 @@ def csa2_index_topk(dims: Dims, cache: Cache, idx_q, w, q_pos, out_idx, out_cnt,
     _check(lib().csa2_index_topk(C.byref(dims), C.byref(cache), ptr(idx_q), ptr(w), ptr(q_pos), ptr(pool),
                                  ptr(pool_cnt), ptr(out_idx), ptr(out_cnt), ptr(out_pool), ptr(out_pool_cnt),
                                  max_entries, ptr(ws), ws.numel() * ws.element_size(), stream_handle(stream)))
+
+
+def csa2_index_topk_noalloc_capacity() -> int:
+    return lib().csa2_index_topk_noalloc_capacity()
+
+
+def csa2_index_topk_noalloc(dims: Dims, cache: Cache, idx_q, w, q_pos, out_idx, out_cnt, max_entries,
+                            pool=None, pool_cnt=None, out_pool=None, out_pool_cnt=None, stream=None):
+    """csa2_index_topk for callers that cannot allocate: scratch is the library's fixed device array."""
+    _check(lib().csa2_index_topk_noalloc(C.byref(dims), C.byref(cache), ptr(idx_q), ptr(w), ptr(q_pos), ptr(pool),
+                                         ptr(pool_cnt), ptr(out_idx), ptr(out_cnt), ptr(out_pool),
+                                         ptr(out_pool_cnt), max_entries, stream_handle(stream)))
 
 
 def csa2_sparse_attn(dims: Dims, cache: Cache, window: Window, Q, q_pos, idx, cnt, softmax_scale, O,

@@ -400,6 +400,22 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   return CSA2_OK;
 }
 
+}  // extern "C"
+
+namespace csa2 {
+int index_topk_into(const csa2_dims* dm, const csa2_cache* c, const void* idx_q, const float* w,
+                    const int32_t* q_pos, const int32_t* pool, const int32_t* pool_cnt, int32_t* out_idx,
+                    int32_t* out_cnt, int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries, void* ws,
+                    size_t ws_bytes, cudaStream_t s) {
+  g_err[0] = 0;
+  return index_topk_impl(dm, c, idx_q, w, q_pos, pool, pool_cnt, out_idx, out_cnt, out_pool, out_pool_cnt,
+                         max_entries, ws, ws_bytes, s);
+}
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace csa2
+
+extern "C" {
+
 int csa2_index_topk(const csa2_dims* dm, const csa2_cache* c, const void* idx_q, const float* w,
                     const int32_t* q_pos, const int32_t* pool, const int32_t* pool_cnt, int32_t* out_idx,
                     int32_t* out_cnt, int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries,

@@ -10,6 +10,14 @@
 
 namespace csa2 {
 
+// csa2_index_topk with caller-chosen scratch (used by the no-allocation entry point).
+int index_topk_into(const csa2_dims* dm, const csa2_cache* c, const void* idx_q, const float* w,
+                    const int32_t* q_pos, const int32_t* pool, const int32_t* pool_cnt, int32_t* out_idx,
+                    int32_t* out_cnt, int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries, void* ws,
+                    size_t ws_bytes, cudaStream_t s);
+// Records `msg` as the calling thread's last error and returns `code`.
+int report_error(int code, const char* msg);
+
 // Device status word of the current device (see csa2_get_status).
 uint32_t* status_word();
 

@@ -1,0 +1,69 @@
+// Indexer + Top-K for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code running inside a CUDA
+// graph being captured, a host thread of a serving loop that must never
+// block on the allocator, or an embedding that owns every byte of the device
+// heap and hands out only fixed buffers.  For them this file keeps the
+// scratch that csa2_index_topk needs (score rows, block maxima, valid counts,
+// key histograms) in one file-scope device array of fixed size.  The array
+// exists once per GPU that loads the library and lives until the process
+// exits; every call shares it.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace csa2 {
+
+// 8 MiB: enough for, e.g., 32 decode rows over 32,768 entries each.
+constexpr size_t kNoAllocScratchBytes = 8u << 20;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of the array for the current device, looked up once per
+// device (with that device current) and cached.  Returns nullptr on failure.
+static void* noalloc_scratch_address(cudaError_t* err) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" size_t csa2_index_topk_noalloc_capacity(void) { return kNoAllocScratchBytes; }
+
+extern "C" int csa2_index_topk_noalloc(const csa2_dims* dims, const csa2_cache* cache, const void* idx_q,
+                                       const float* w, const int32_t* q_pos, const int32_t* pool,
+                                       const int32_t* pool_cnt, int32_t* out_idx, int32_t* out_cnt,
+                                       int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries,
+                                       void* stream) {
+  if (!dims) return report_error(CSA2_ERR_INVALID_ARG, "dims must not be NULL");
+  const size_t need = csa2_index_topk_workspace_size(dims, max_entries);
+  if (need > kNoAllocScratchBytes)
+    return report_error(CSA2_ERR_WORKSPACE,
+                        "csa2_index_topk_noalloc: this shape needs more scratch than the fixed 8 MiB "
+                        "device array (check csa2_index_topk_workspace_size); use csa2_index_topk with "
+                        "a caller-allocated workspace instead");
+  cudaError_t e = cudaSuccess;
+  void* scratch = noalloc_scratch_address(&e);
+  if (!scratch) return report_error(CSA2_ERR_CUDA, "csa2_index_topk_noalloc: cudaGetSymbolAddress failed");
+  // the histogram part of the scratch is cleared by the call itself; the rest
+  // is written before it is read
+  return index_topk_into(dims, cache, idx_q, w, q_pos, pool, pool_cnt, out_idx, out_cnt, out_pool,
+                         out_pool_cnt, max_entries, scratch, kNoAllocScratchBytes,
+                         static_cast<cudaStream_t>(stream));
+}

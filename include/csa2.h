@@ -249,6 +249,28 @@ int csa2_index_topk(const csa2_dims* dims, const csa2_cache* cache, const void* 
                     int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* ---- csa2_index_topk without a caller workspace ---------------------------
+ * No counterpart in the paper: a convenience for callers that cannot
+ * allocate device memory (for example code that runs while a CUDA graph is
+ * being captured, or a serving thread that must never wait on the
+ * allocator).  Same arguments and results as csa2_index_topk, but the scratch
+ * lives in one fixed 8 MiB array inside the library
+ * (csa2_index_topk_noalloc_capacity() bytes), held by every GPU that loads
+ * the library until the process exits.  Shapes whose
+ * csa2_index_topk_workspace_size() exceeds it are rejected with
+ * CSA2_ERR_WORKSPACE.  The first call on a device looks the array's device
+ * address up (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  The call clears the part of the array that
+ * must start at zero.  All calls share the one array: calls that can overlap
+ * on the GPU (different streams without ordering between them) race and give
+ * wrong results; order them on one stream.  Allocates nothing. */
+size_t csa2_index_topk_noalloc_capacity(void);
+int csa2_index_topk_noalloc(const csa2_dims* dims, const csa2_cache* cache, const void* idx_q,
+                            const float* w, const int32_t* q_pos, const int32_t* pool,
+                            const int32_t* pool_cnt, int32_t* out_idx, int32_t* out_cnt,
+                            int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries,
+                            void* stream);
+
 /* ---- a11: gathered sparse MQA attention + FP8 window (R11) ----------------
  * Q bf16 [B][Tq][Hq][d] (already rotated at its own position); idx int32
  * [B][Tq][K] (-1 padded) with cnt int32 [B][Tq]; O fp32 [B][Tq][Hq][d];
