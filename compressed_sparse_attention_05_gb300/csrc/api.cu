@@ -123,8 +123,11 @@ static IndexerArgs indexer_args(const csa2_dims* dm, const csa2_cache* c, const 
 // Workspace of csa2_index_topk: scores, block maxima, valid counts.
 constexpr int kHistBins = 2048;  // score-key histogram bins per row (top 11 key bits)
 
+// Rows up to this count take the split Top-K (many CTAs per row).
+constexpr int64_t kSplitTopkMaxRows = 256;
+
 struct IndexWs {
-  size_t scores_off, bm_off, nvalid_off, hist_off, total;
+  size_t scores_off, bm_off, nvalid_off, hist_off, split_off, total;
   int64_t s_stride, bm_stride;
 };
 static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
@@ -140,7 +143,9 @@ static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
   L.bm_off = round_up(L.scores_off + (size_t)(rows * L.s_stride) * 4, 256);
   L.nvalid_off = round_up(L.bm_off + (size_t)(rows * L.bm_stride) * 4, 256);
   L.hist_off = round_up(L.nvalid_off + (size_t)rows * 4, 256);
-  L.total = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
+  L.split_off = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
+  const size_t split = rows <= kSplitTopkMaxRows ? topk_split_scratch_bytes(rows, L.s_stride) : 0;
+  L.total = round_up(L.split_off + split, 256);
   return L;
 }
 
@@ -290,8 +295,9 @@ int csa2_index_scores(const csa2_dims* dm, const csa2_cache* c, const void* idx_
 }
 
 size_t csa2_topk_workspace_size(int64_t rows, int64_t stride, int32_t k) {
-  (void)rows; (void)stride; (void)k;
-  return 0;
+  (void)k;
+  if (rows <= 0 || stride <= 0) return 0;
+  return round_up((size_t)rows * kHistBins * 4, 256) + topk_split_scratch_bytes(rows, stride);
 }
 
 int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32_t* n_valid, int32_t k,
@@ -305,9 +311,19 @@ int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32
   REQUIRE_PTR(scores); REQUIRE_IPTR(out_idx); REQUIRE_IPTR(out_cnt);
   if (n_valid) REQUIRE_IPTR(n_valid);
   ValidSpec v{n_valid, nullptr, nullptr, 1, 1, 0};
-  LAUNCH(launch_topk(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, nullptr, 0,
-                     static_cast<cudaStream_t>(stream)),
-         "topk");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t need = csa2_topk_workspace_size(rows, stride, k);
+  if (ws && ws_bytes >= need) {   // many CTAs per row
+    REQUIRE(aligned16(ws), "ws must be 16-byte aligned");
+    uint32_t* hist = static_cast<uint32_t*>(ws);
+    char* split = static_cast<char*>(ws) + round_up((size_t)rows * kHistBins * 4, 256);
+    LAUNCH(launch_row_hist(scores, rows, stride, v, hist, s), "row_hist");
+    LAUNCH(launch_topk_split(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins,
+                             split, s),
+           "topk_split");
+    return CSA2_OK;
+  }
+  LAUNCH(launch_topk(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, nullptr, 0, s), "topk");
   return CSA2_OK;
 }
 
@@ -381,8 +397,14 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
     LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s),
            "index_scores");
     ValidSpec v{nullptr, c->n_entries, q_pos, dm->Tq, 1, max_entries};
-    LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins, s),
-           "topk");
+    if (rows <= kSplitTopkMaxRows)
+      LAUNCH(launch_topk_split(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist,
+                               kHistBins, base + L.split_off, s),
+             "topk");
+    else
+      LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins,
+                         s),
+             "topk");
     if (out_pool) {
       ValidSpec vb{nullptr, c->n_entries, q_pos, dm->Tq, 8, max_entries};
       LAUNCH(launch_topk(bm, rows, L.bm_stride, vb, dm->n_pool_blocks, out_pool, out_pool_cnt,

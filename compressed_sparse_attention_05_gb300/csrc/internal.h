@@ -109,6 +109,15 @@ struct Remap {
 cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
                         int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
                         int64_t hist_stride, cudaStream_t s);
+// Split Top-K for few rows: many CTAs per row collect, one CTA per row
+// finishes.  Needs the row histograms and topk_split_scratch_bytes of scratch.
+size_t topk_split_scratch_bytes(int64_t rows, int64_t stride);
+// Per-row 2048-bin histograms of the top 11 key bits of given scores (zeroed first).
+cudaError_t launch_row_hist(const float* scores, int64_t rows, int64_t stride, ValidSpec v, uint32_t* hist,
+                            cudaStream_t s);
+cudaError_t launch_topk_split(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
+                              int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
+                              int64_t hist_stride, void* scratch, cudaStream_t s);
 // Block maxima of the valid columns: out[row][b] = max(scores[row][block*b ..]).
 cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, ValidSpec v,
                              int block, float* out, int64_t out_stride, cudaStream_t s);

@@ -53,8 +53,10 @@ __device__ __forceinline__ int32_t remap_index(const Remap& r, int64_t row, int 
   return r.pool[row * r.pool_stride + c / r.block] * r.block + c % r.block;
 }
 
-// Exclusive block-wide prefix sum of one int per thread.
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
+// Exclusive block-wide prefix sum of one int per thread (NT threads).
+template <int NT>
+__device__ __forceinline__ int block_exclusive_scan_t(int v, int* warp_tot) {
+  constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -65,18 +67,21 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   if (lane == 31) warp_tot[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kTopkWarps ? warp_tot[lane] : 0;
+    int w = lane < NW ? warp_tot[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    if (lane < kTopkWarps) warp_tot[lane] = w;
+    if (lane < NW) warp_tot[lane] = w;
   }
   __syncthreads();
   const int before = warp ? warp_tot[warp - 1] : 0;
   __syncthreads();
   return before + x - v;
+}
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
+  return block_exclusive_scan_t<kTopkThreads>(v, warp_tot);
 }
 
 // Adds `digit` (< nbins, or >= nbins for "none") to a shared histogram with
@@ -101,15 +106,16 @@ __device__ __forceinline__ int warp_slot(int* counter, bool take, int cap) {
 
 // Finds, scanning digits from the top, the digit holding the need-th largest
 // element of a `bins`-bin histogram; *above receives the count in higher bins.
-__device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int need, int* warp_tot, int* above) {
+template <int NT>
+__device__ __forceinline__ int find_digit_t(const uint32_t* hist, int bins, int need, int* warp_tot, int* above) {
   __shared__ int s_digit, s_above;
-  const int per = (bins + kTopkThreads - 1) / kTopkThreads;
+  const int per = (bins + NT - 1) / NT;
   const int hi = bins - (int)threadIdx.x * per;   // thread t owns [hi - per, hi), highest first
   const int lo = max(0, hi - per);
   int c = 0;
   for (int d = lo; d < hi; ++d) c += hist[d];
   if (threadIdx.x == 0) { s_digit = 0; s_above = 0; }
-  const int before = block_exclusive_scan(c, warp_tot);
+  const int before = block_exclusive_scan_t<NT>(c, warp_tot);
   if (before < need && before + c >= need) {
     int cum = before;
     for (int d = hi - 1; d >= lo; --d) {
@@ -126,6 +132,9 @@ __device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int ne
   *above = s_above;
   return s_digit;
 }
+__device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int need, int* warp_tot, int* above) {
+  return find_digit_t<kTopkThreads>(hist, bins, need, warp_tot, above);
+}
 
 constexpr int kBitmapMax = 1 << 18;            // rows up to 262,144 entries use bitmaps
 constexpr int kBitmapWords = kBitmapMax / 32;
@@ -141,143 +150,78 @@ struct TopkSmem {
   uint32_t tie_bits[kBitmapWords];  // entries equal to the K-th key
 };
 
-__global__ void __launch_bounds__(kTopkThreads)
-k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
-       int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
-  const int64_t row = blockIdx.x;
-  const float* s = scores + row * stride;
-  const int n = row_valid(v, row, stride);
-  const int kk = min(k, n);
-  int32_t* out = out_idx + row * (int64_t)k;
-  const int tid = threadIdx.x, lane = tid & 31;
-
-  for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
-  if (tid == 0) out_cnt[row] = kk;
-  if (kk == 0) return;
-  if (kk == n) {  // everything visible is selected
-    for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
-    return;
-  }
-
-  // ---- histogram of the top 11 key bits
-  if (hist_in) {
-    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
-  } else {
-    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
+// Selection from the candidates of the threshold bin: the sel bitmap already
+// holds every entry of a higher bin; find the exact K-th key among the
+// candidates, mark the candidates above it and the `need` lowest-index ties,
+// and write the selection in index order.
+__device__ void finish_from_candidates(TopkSmem& sm, int n, int kk, int bstar, int need, int nC,
+                                       int32_t* __restrict__ out, const Remap& remap, int64_t row) {
+  const int tid = threadIdx.x;
+  const int words = (n + 31) / 32;
+  uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
+  for (int p = 0; p < 3; ++p) {   // 3 radix passes of 7 bits over the candidates
+    const int sh = 14 - 7 * p;
+    const uint32_t nb = 128;
+    for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
     __syncthreads();
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
-      float v[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {   // independent loads first
-        const int j = j0 + u * kTopkThreads + tid;
-        v[u] = j < n ? s[j] : 0.f;
+    for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
+      const int i = i0 + tid;
+      uint32_t dg = 0xFFFFFFFFu;
+      if (i < nC) {
+        const uint32_t key = sm.ckey[i];
+        if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
       }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        warp_hist_add(sm.hist, j < n ? order_key(v[u]) >> 21 : 0xFFFFFFFFu, 2048);
-      }
+      warp_hist_add(sm.hist2, dg, nb);
     }
+    __syncthreads();
+    int ab;
+    const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+    need -= ab;
+    prefix |= (uint32_t)dg << sh;
+    mask |= (nb - 1) << sh;
   }
-  if (tid == 0) sm.nC = 0;
+  const uint32_t T = prefix;             // exact K-th key; `need` entries equal to T are taken
+  for (int i = tid; i < nC; i += kTopkThreads) {
+    const uint32_t key = sm.ckey[i];
+    const int32_t j = sm.cidx[i];
+    if (key > T) atomicOr(&sm.sel_bits[j >> 5], 1u << (j & 31));
+    else if (key == T) atomicOr(&sm.tie_bits[j >> 5], 1u << (j & 31));
+  }
   __syncthreads();
-  int above;
-  const int bstar = find_digit(sm.hist, 2048, kk, sm.warp_tot, &above);
-  int need = kk - above;                  // entries of bin bstar to take
-  const int n_bin = (int)sm.hist[bstar];
-
-  if (n_bin <= kCandCap && n <= kBitmapMax) {
-    const int words = (n + 31) / 32;
-    for (int i = tid; i < words; i += kTopkThreads) sm.tie_bits[i] = 0;
-    // ---- one pass: higher bins -> selection bitmap; bin bstar -> candidate list
-    // (lanes of a warp cover one aligned 32-entry word, so the ballot is the word)
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
-      float v[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {   // independent loads first
-        const int j = j0 + u * kTopkThreads + tid;
-        v[u] = j < n ? s[j] : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int j = j0 + u * kTopkThreads + tid;
-        uint32_t key = 0, bin = 0;
-        if (j < n) {
-          key = order_key(v[u]);
-          bin = key >> 21;
-        }
-        const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
-        if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
-        const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
-        if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
-      }
+  // index-ordered output: thread tid owns words [w0, w1)
+  const int per = (words + kTopkThreads - 1) / kTopkThreads;
+  const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
+  int ties = 0;
+  for (int w = w0; w < w1; ++w) ties += __popc(sm.tie_bits[w]);
+  int ties_before = block_exclusive_scan(ties, sm.warp_tot);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t tb = sm.tie_bits[w];
+    while (tb && ties_before < need) {      // lowest indices first
+      const uint32_t low = tb & (0u - tb);
+      sm.sel_bits[w] |= low;
+      tb ^= low;
+      ++ties_before;
     }
-    __syncthreads();
-    const int nC = min(sm.nC, kCandCap);
-    // ---- exact threshold among the candidates: 3 radix passes over 21 bits
-    uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
-    for (int p = 0; p < 3; ++p) {
-      const int sh = 14 - 7 * p;
-      const uint32_t nb = 128;
-      for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
-      __syncthreads();
-      for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
-        const int i = i0 + tid;
-        uint32_t dg = 0xFFFFFFFFu;
-        if (i < nC) {
-          const uint32_t key = sm.ckey[i];
-          if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
-        }
-        warp_hist_add(sm.hist2, dg, nb);
-      }
-      __syncthreads();
-      int ab;
-      const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
-      need -= ab;
-      prefix |= (uint32_t)dg << sh;
-      mask |= (nb - 1) << sh;
-    }
-    const uint32_t T = prefix;             // exact K-th key; `need` entries equal to T are taken
-    for (int i = tid; i < nC; i += kTopkThreads) {
-      const uint32_t key = sm.ckey[i];
-      const int32_t j = sm.cidx[i];
-      if (key > T) atomicOr(&sm.sel_bits[j >> 5], 1u << (j & 31));
-      else if (key == T) atomicOr(&sm.tie_bits[j >> 5], 1u << (j & 31));
-    }
-    __syncthreads();
-    // ---- index-ordered output: thread tid owns words [w0, w1)
-    const int per = (words + kTopkThreads - 1) / kTopkThreads;
-    const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
-    int ties = 0;
-    for (int w = w0; w < w1; ++w) ties += __popc(sm.tie_bits[w]);
-    int ties_before = block_exclusive_scan(ties, sm.warp_tot);
-    int cnt = 0;
-    for (int w = w0; w < w1; ++w) {
-      uint32_t tb = sm.tie_bits[w];
-      while (tb && ties_before < need) {      // lowest indices first
-        const uint32_t low = tb & (0u - tb);
-        sm.sel_bits[w] |= low;
-        tb ^= low;
-        ++ties_before;
-      }
-      cnt += __popc(sm.sel_bits[w]);
-    }
-    int pos = block_exclusive_scan(cnt, sm.warp_tot);
-    for (int w = w0; w < w1; ++w) {
-      uint32_t sb = sm.sel_bits[w];
-      while (sb) {
-        const int bit = __ffs(sb) - 1;
-        sb &= sb - 1;
-        if (pos < kk) out[pos] = remap_index(remap, row, w * 32 + bit);
-        ++pos;
-      }
-    }
-    return;
+    cnt += __popc(sm.sel_bits[w]);
   }
+  int pos = block_exclusive_scan(cnt, sm.warp_tot);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t sb = sm.sel_bits[w];
+    while (sb) {
+      const int bit = __ffs(sb) - 1;
+      sb &= sb - 1;
+      if (pos < kk) out[pos] = remap_index(remap, row, w * 32 + bit);
+      ++pos;
+    }
+  }
+}
 
-  // ---- crowded threshold bin: radix select over the row from the 11-bit prefix
+// Crowded threshold bin: radix select over the whole row from the 11-bit
+// prefix, then an index-ordered pass writes the selection.
+__device__ void radix_whole_row(TopkSmem& sm, const float* __restrict__ s, int n, int kk, int bstar, int need,
+                                int32_t* __restrict__ out, const Remap& remap, int64_t row) {
+  const int tid = threadIdx.x;
   uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
   for (int p = 0; p < 3; ++p) {
     const int sh = p == 0 ? 13 : (p == 1 ? 5 : 0);
@@ -301,7 +245,6 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
     mask |= (nb - 1) << sh;
   }
   const uint32_t T = prefix;
-  // index-ordered output: thread tid owns columns [lo, hi)
   const int chunk = (n + kTopkThreads - 1) / kTopkThreads;
   const int lo = min(n, tid * chunk), hi = min(n, lo + chunk);
   int gt = 0, eq = 0;
@@ -327,6 +270,265 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
       ++eq_seen;
     }
   }
+}
+
+// Loads (or builds) the 2048-bin key histogram of a row into shared memory
+// and locates the threshold bin.
+template <int NT>
+__device__ __forceinline__ void locate_bin(uint32_t* shist, int* warp_tot, const float* __restrict__ s, int n,
+                                           int kk, const uint32_t* __restrict__ hist_row, int* bstar, int* above) {
+  const int tid = threadIdx.x;
+  if (hist_row) {
+    for (int i = tid; i < 2048; i += NT) shist[i] = hist_row[i];
+  } else {
+    for (int i = tid; i < 2048; i += NT) shist[i] = 0;
+    __syncthreads();
+    for (int j0 = 0; j0 < n; j0 += NT * kBatch) {
+      float v[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {   // independent loads first
+        const int j = j0 + u * NT + tid;
+        v[u] = j < n ? s[j] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int j = j0 + u * NT + tid;
+        warp_hist_add(shist, j < n ? order_key(v[u]) >> 21 : 0xFFFFFFFFu, 2048);
+      }
+    }
+  }
+  __syncthreads();
+  *bstar = find_digit_t<NT>(shist, 2048, kk, warp_tot, above);
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+       int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int64_t row = blockIdx.x;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);
+  const int kk = min(k, n);
+  int32_t* out = out_idx + row * (int64_t)k;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
+  if (tid == 0) out_cnt[row] = kk;
+  if (kk == 0) return;
+  if (kk == n) {  // everything visible is selected
+    for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
+    return;
+  }
+  if (tid == 0) sm.nC = 0;
+  int bstar, above;
+  locate_bin<kTopkThreads>(sm.hist, sm.warp_tot, s, n, kk, hist_in ? hist_in + row * hist_stride : nullptr,
+                           &bstar, &above);
+  const int need = kk - above;           // entries of bin bstar to take
+  const int n_bin = (int)sm.hist[bstar];
+  if (n_bin > kCandCap || n > kBitmapMax) {
+    radix_whole_row(sm, s, n, kk, bstar, need, out, remap, row);
+    return;
+  }
+  const int words = (n + 31) / 32;
+  for (int i = tid; i < words; i += kTopkThreads) sm.tie_bits[i] = 0;
+  // one pass: higher bins -> selection bitmap; bin bstar -> candidate list
+  // (lanes of a warp cover one aligned 32-entry word, so the ballot is the word)
+  for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
+    float vv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {   // independent loads first
+      const int j = j0 + u * kTopkThreads + tid;
+      vv[u] = j < n ? s[j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kTopkThreads + tid;
+      uint32_t key = 0, bin = 0;
+      if (j < n) {
+        key = order_key(vv[u]);
+        bin = key >> 21;
+      }
+      const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
+      if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
+      const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
+      if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
+    }
+  }
+  __syncthreads();
+  finish_from_candidates(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
+}
+
+// ---- split Top-K: few, long rows ---------------------------------------------------
+// The collection pass of k_topk spread over many CTAs per row: every CTA
+// locates the threshold bin from the row histogram itself, then for its chunk
+// of 4,096 entries writes the selection-bitmap words of the higher bins and
+// appends the threshold bin's candidates to a per-row list in scratch.  One
+// CTA per row then finishes from the candidates (k_topk_finish).
+constexpr int kCollectThreads = 256;
+constexpr int kCollectChunk = 4096;
+
+__global__ void __launch_bounds__(kCollectThreads)
+k_topk_collect(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k,
+               const uint32_t* __restrict__ hist_in, int64_t hist_stride, uint32_t* __restrict__ sel_words,
+               int64_t words_stride, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx,
+               int32_t* __restrict__ cand_count) {
+  __shared__ uint32_t shist[2048];
+  __shared__ int warp_tot[kCollectThreads / 32];
+  const int64_t row = blockIdx.y;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);
+  const int kk = min(k, n);
+  const int c0 = blockIdx.x * kCollectChunk;
+  if (kk == 0 || kk == n || c0 >= n || n > kBitmapMax) return;
+  int bstar, above;
+  locate_bin<kCollectThreads>(shist, warp_tot, s, n, kk, hist_in + row * hist_stride, &bstar, &above);
+  if ((int)shist[bstar] > kCandCap) return;       // the finish kernel takes the whole-row path
+  const int c1 = min(n, c0 + kCollectChunk);
+  const int tid = threadIdx.x, lane = tid & 31;
+  for (int j0 = c0; j0 < c1; j0 += kCollectThreads * kBatch) {
+    float vv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kCollectThreads + tid;
+      vv[u] = j < c1 ? s[j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kCollectThreads + tid;
+      uint32_t key = 0, bin = 0;
+      if (j < c1) {
+        key = order_key(vv[u]);
+        bin = key >> 21;
+      }
+      const uint32_t word = __ballot_sync(0xffffffffu, j < c1 && bin > (uint32_t)bstar);
+      if (lane == 0 && j < c1) sel_words[row * words_stride + (j >> 5)] = word;
+      const bool cand = j < c1 && bin == (uint32_t)bstar;
+      const uint32_t m = __ballot_sync(0xffffffffu, cand);
+      if (m) {
+        int base = 0;
+        if (lane == __ffs(m) - 1) base = atomicAdd(&cand_count[row], __popc(m));
+        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+        const int pos = base + __popc(m & ((1u << lane) - 1));
+        if (cand && pos < kCandCap) {
+          cand_key[row * kCandCap + pos] = key;
+          cand_idx[row * kCandCap + pos] = j;
+        }
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkThreads)
+k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+              int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride,
+              const uint32_t* __restrict__ sel_words, int64_t words_stride, const uint32_t* __restrict__ cand_key,
+              const int32_t* __restrict__ cand_idx, const int32_t* __restrict__ cand_count) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int64_t row = blockIdx.x;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);
+  const int kk = min(k, n);
+  int32_t* out = out_idx + row * (int64_t)k;
+  const int tid = threadIdx.x;
+  for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
+  if (tid == 0) out_cnt[row] = kk;
+  if (kk == 0) return;
+  if (kk == n) {
+    for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
+    return;
+  }
+  int bstar, above;
+  locate_bin<kTopkThreads>(sm.hist, sm.warp_tot, s, n, kk, hist_in + row * hist_stride, &bstar, &above);
+  const int need = kk - above;
+  if ((int)sm.hist[bstar] > kCandCap || n > kBitmapMax) {
+    radix_whole_row(sm, s, n, kk, bstar, need, out, remap, row);
+    return;
+  }
+  const int words = (n + 31) / 32;
+  const int nC = min(cand_count[row], kCandCap);
+  for (int i = tid; i < words; i += kTopkThreads) {
+    sm.sel_bits[i] = sel_words[row * words_stride + i];
+    sm.tie_bits[i] = 0;
+  }
+  for (int i = tid; i < nC; i += kTopkThreads) {
+    sm.ckey[i] = cand_key[row * kCandCap + i];
+    sm.cidx[i] = cand_idx[row * kCandCap + i];
+  }
+  __syncthreads();
+  finish_from_candidates(sm, n, kk, bstar, need, nC, out, remap, row);
+}
+
+// 2048-bin key histograms of given score rows (for the split path on a given array).
+__global__ void __launch_bounds__(kCollectThreads)
+k_row_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, uint32_t* __restrict__ hist) {
+  __shared__ uint32_t sh[2048];
+  const int64_t row = blockIdx.y;
+  const int n = row_valid(v, row, stride);
+  const int c0 = blockIdx.x * kCollectChunk;
+  if (c0 >= n) return;
+  const int c1 = min(n, c0 + kCollectChunk);
+  for (int i = threadIdx.x; i < 2048; i += kCollectThreads) sh[i] = 0;
+  __syncthreads();
+  const float* s = scores + row * stride;
+  for (int j0 = c0; j0 < c1; j0 += kCollectThreads * kBatch) {
+    float vv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kCollectThreads + threadIdx.x;
+      vv[u] = j < c1 ? s[j] : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kCollectThreads + threadIdx.x;
+      warp_hist_add(sh, j < c1 ? order_key(vv[u]) >> 21 : 0xFFFFFFFFu, 2048);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 2048; i += kCollectThreads)
+    if (sh[i]) atomicAdd(&hist[row * 2048 + i], sh[i]);
+}
+
+cudaError_t launch_row_hist(const float* scores, int64_t rows, int64_t stride, ValidSpec v, uint32_t* hist,
+                            cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)rows * 2048 * 4, s);
+  if (e != cudaSuccess) return e;
+  dim3 g((unsigned)((stride + kCollectChunk - 1) / kCollectChunk), (unsigned)rows);
+  k_row_hist<<<g, kCollectThreads, 0, s>>>(scores, stride, v, hist);
+  return counted(cudaGetLastError());
+}
+
+size_t topk_split_scratch_bytes(int64_t rows, int64_t stride) {
+  const int64_t words = (stride + 31) / 32;
+  return (size_t)rows * (words * 4 + (int64_t)kCandCap * 8 + 16);
+}
+
+cudaError_t launch_topk_split(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
+                              int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
+                              int64_t hist_stride, void* scratch, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  const int64_t words = (stride + 31) / 32;
+  char* p = static_cast<char*>(scratch);
+  uint32_t* cand_key = reinterpret_cast<uint32_t*>(p);
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(p + (size_t)rows * kCandCap * 4);
+  int32_t* cand_count = reinterpret_cast<int32_t*>(p + (size_t)rows * kCandCap * 8);
+  uint32_t* sel_words = reinterpret_cast<uint32_t*>(p + (size_t)rows * kCandCap * 8 + (size_t)rows * 16);
+  cudaError_t e = cudaMemsetAsync(cand_count, 0, (size_t)rows * 16, s);
+  if (e != cudaSuccess) return e;
+  dim3 g1((unsigned)((stride + kCollectChunk - 1) / kCollectChunk), (unsigned)rows);
+  k_topk_collect<<<g1, kCollectThreads, 0, s>>>(scores, stride, v, k, hist, hist_stride, sel_words, words,
+                                                cand_key, cand_idx, cand_count);
+  e = counted(cudaGetLastError());
+  if (e != cudaSuccess) return e;
+  const size_t smem = sizeof(TopkSmem);
+  e = cudaFuncSetAttribute(k_topk_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_topk_finish<<<(unsigned)rows, kTopkThreads, smem, s>>>(scores, stride, v, k, out_idx, out_cnt, remap, hist,
+                                                           hist_stride, sel_words, words, cand_key, cand_idx,
+                                                           cand_count);
+  return counted(cudaGetLastError());
 }
 
 // Block maxima: out[row][b] = max of scores[row][8b .. 8b+7] over the valid

@@ -222,7 +222,9 @@ int csa2_index_scores(const csa2_dims* dims, const csa2_cache* cache, const void
 /* ---- a6: Top-K of a given fp32 array (bit-exact contract, R8) -------------
  * scores fp32 [rows][stride]; n_valid int32 [rows] (device) or NULL (all
  * `stride` columns valid).  out_idx int32 [rows][k] ascending, -1 padded;
- * out_cnt int32 [rows].  k in 1..4096; stride < 2^31. */
+ * out_cnt int32 [rows].  k in 1..4096; stride < 2^31.  With a workspace of
+ * csa2_topk_workspace_size() bytes each row is spread over many CTAs (for few,
+ * long rows); with ws == NULL one CTA handles each row.  Same result. */
 size_t csa2_topk_workspace_size(int64_t rows, int64_t stride, int32_t k);
 int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32_t* n_valid,
                   int32_t k, int32_t* out_idx, int32_t* out_cnt, void* ws, size_t ws_bytes,

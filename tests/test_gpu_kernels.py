@@ -126,13 +126,17 @@ def _score_rows():
     return torch.stack(rows).contiguous(), torch.tensor(n_valid, dtype=torch.int32)
 
 
+@pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("k", [512, 16, 2048, 1])
-def test_topk_bit_exact(k):
+def test_topk_bit_exact(k, split):
     s, nv = _score_rows()
     rows = s.shape[0]
     idx = torch.full((rows, k), -5, dtype=torch.int32, device="cuda")
     cnt = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
-    abi.csa2_topk_f32(s.cuda(), nv.cuda(), k, idx, cnt)
+    ws = None
+    if split:   # many CTAs per row
+        ws = torch.empty(abi.csa2_topk_workspace_size(rows, s.shape[1], k), dtype=torch.uint8, device="cuda")
+    abi.csa2_topk_f32(s.cuda(), nv.cuda(), k, idx, cnt, ws=ws)
     idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
     for r in range(rows):
         ref = I.topk(s[r, :nv[r]].numpy(), k)
