@@ -300,6 +300,239 @@ k_sparse_attn(AttnArgs a, uint32_t* status) {
   }
 }
 
+// ---- register-prefetch variant (d = 512) -------------------------------------------
+// Same tiling and math as k_sparse_attn, with the gather latency taken off the
+// critical path: every key's source (pool slot or window row) is resolved
+// once at the start, and the packed bytes of tile t+1 (each thread: 8 groups
+// of 16 channels) are loaded into registers while tile t runs its tensor-core
+// phases.  90 KB of shared memory keeps two CTAs per SM.
+__global__ void __launch_bounds__(kAttnThreads, 2)
+k_sparse_attn_rp(AttnArgs a, uint32_t* status) {
+  constexpr int D = 512;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  AttnSmem<D>& sm = *reinterpret_cast<AttnSmem<D>*>(smem_raw);
+  int64_t* slots = reinterpret_cast<int64_t*>(smem_raw + sizeof(AttnSmem<D>));
+  constexpr int QS = AttnSmem<D>::QS, PS = AttnSmem<D>::PS;
+  constexpr int DW = D / kAttnWarps, NT = DW / 8;
+  constexpr int kItems = kTK * (D / 16) / kAttnThreads;   // 8 groups per thread per tile
+  const int64_t row = blockIdx.y;
+  const int hg = blockIdx.x;
+  const int b = (int)(row / a.Tq);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+
+  const int t = a.q_pos[row];
+  const int nv = n_visible(a.n_entries[b], t);
+  int n_sel = a.cnt[row];
+  if (n_sel < 0 || n_sel > a.K) {
+    if (tid == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    n_sel = n_sel < 0 ? 0 : a.K;
+  }
+  const int pos0 = a.swa_cap > 0 ? a.swa_pos0[b] : 0;
+  const int w_lo = max(max(0, t - a.W + 1), pos0);
+  const int w_hi = min(t, pos0 + a.swa_cap - 1);
+  const int n_win = max(0, w_hi - w_lo + 1);
+  const int n_keys = n_sel + n_win;
+  const int n_tiles = (n_keys + kTK - 1) / kTK;
+
+  for (int i = tid; i < n_keys; i += kAttnThreads) {
+    int64_t sv;
+    if (i < n_sel) {
+      const int j = a.idx[row * a.K + i];
+      sv = -1;
+      if (j >= 0 && j < nv) sv = entry_slot(a.page_table, a.max_pages, a.n_pages, b, j, status);
+      else raise_status(status, CSA2_STATUS_BAD_INDEX);
+    } else {
+      sv = -2 - (int64_t)(w_lo + (i - n_sel) - pos0);
+    }
+    slots[i] = sv;
+  }
+  for (int i = tid; i < kHG * (D / 8); i += kAttnThreads) {
+    const int h = i / (D / 8), c8 = i % (D / 8);
+    const int head = hg * kHG + h;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (head < a.Hq) {
+      const uint4 qb = *reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + head) * D + c8 * 8);
+      const uint32_t qw[4] = {qb.x, qb.y, qb.z, qb.w};
+      uint32_t ov[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ov[j] = f32_to_f16_bits(bf16_bits_to_f32(qw[j] & 0xFFFFu)) |
+                (f32_to_f16_bits(bf16_bits_to_f32(qw[j] >> 16)) << 16);
+      v = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+    }
+    *reinterpret_cast<uint4*>(&sm.q[h * QS + c8 * 8]) = v;
+  }
+  if (tid < kHG) {
+    sm.m[tid] = -INFINITY;
+    sm.l[tid] = 0.f;
+  }
+  __syncthreads();
+
+  // item u of this thread: key (tid / 32) + 8u of the tile, group tid % 32
+  const int grp = tid & 31;
+  uint4 raw[kItems];
+  float rsc[kItems];
+  auto prefetch = [&](int ti) {
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int kr = (tid >> 5) + 8 * u;
+      const int i = ti * kTK + kr;
+      const int64_t src = i < n_keys ? slots[i] : -1;
+      if (src >= 0) {
+        const uint2 c = *reinterpret_cast<const uint2*>(a.kv_codes + src * (D / 2) + grp * 8);
+        raw[u] = make_uint4(c.x, c.y, a.kv_scales[src * (D / 16) + grp], 0);
+      } else if (src <= -2) {
+        const int64_t wr = (int64_t)b * a.swa_cap + (-2 - src);
+        raw[u] = *reinterpret_cast<const uint4*>(a.swa_codes + wr * D + grp * 16);
+        rsc[u] = a.swa_scales[wr];
+      }
+    }
+  };
+
+  float o[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  const float sl2 = a.scale * 1.4426950408889634f;
+  if (n_tiles > 0) prefetch(0);
+
+  for (int ti = 0; ti < n_tiles; ++ti) {
+    // ---- dequantise the prefetched tile
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) {
+      const int kr = (tid >> 5) + 8 * u;
+      const int i = ti * kTK + kr;
+      const int64_t src = i < n_keys ? slots[i] : -1;
+      uint32_t w[8];
+      if (src >= 0) {
+        const uint32_t s2 = f32_to_f16_bits(e4m3_to_f32(raw[u].z)) * 0x10001u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t word = q < 4 ? raw[u].x : raw[u].y;
+          w[q] = hmul2_u32(e2m1x2_to_f16x2((word >> ((q & 3) * 8)) & 0xFFu), s2);
+        }
+      } else if (src <= -2) {
+        const uint32_t cw[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t word = cw[q >> 1];
+          const int sh = (q & 1) * 16;
+          const float lo = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32((word >> sh) & 0xFFu) * rsc[u]));
+          const float hi = bf16_bits_to_f32(f32_to_bf16_bits(e4m3_to_f32((word >> (sh + 8)) & 0xFFu) * rsc[u]));
+          w[q] = f32_to_f16_bits(lo) | (f32_to_f16_bits(hi) << 16);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) w[q] = 0;
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(&sm.k[kr * QS + grp * 16]);
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    __syncthreads();
+    if (ti + 1 < n_tiles) prefetch(ti + 1);   // in flight during the phases below
+    // ---- S = Q K^T : warp owns keys 8*warp .. +7 (four accumulators)
+    {
+      float sa[4][4] = {};
+      const uint32_t qa = smem_u32(&sm.q[(lane & 15) * QS + (lane >> 4) * 8]);
+      const uint32_t kb = smem_u32(&sm.k[(warp * 8 + (lane & 7)) * QS + (lane >> 3) * 8]);
+#pragma unroll
+      for (int ks = 0; ks < D / 32; ks += 2) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint32_t a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3;
+          ldsm_x4(qa + (ks + u) * 64, a0, a1, a2, a3);
+          ldsm_x4(qa + (ks + u) * 64 + 32, a4, a5, a6, a7);
+          ldsm_x4(kb + (ks + u) * 64, b0, b1, b2, b3);
+          mma_f16(sa[2 * u], a0, a1, a2, a3, b0, b1);
+          mma_f16(sa[2 * u + 1], a4, a5, a6, a7, b2, b3);
+        }
+      }
+      const int key0 = warp * 8 + 2 * t4;
+      const int i0 = ti * kTK + key0;
+      const bool v0 = i0 < n_keys && slots[i0] != -1, v1 = i0 + 1 < n_keys && slots[i0 + 1] != -1;
+      float s0[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) s0[r] = (sa[0][r] + sa[1][r]) + (sa[2][r] + sa[3][r]);
+      sm.s[g * kTK + key0] = v0 ? s0[0] * sl2 : -INFINITY;
+      sm.s[g * kTK + key0 + 1] = v1 ? s0[1] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0] = v0 ? s0[2] * sl2 : -INFINITY;
+      sm.s[(g + 8) * kTK + key0 + 1] = v1 ? s0[3] * sl2 : -INFINITY;
+    }
+    __syncthreads();
+    // ---- online softmax: 16 threads per head, 4 keys each
+    {
+      const int h = tid >> 4, part = tid & 15;
+      const float4 sv = *reinterpret_cast<const float4*>(&sm.s[h * kTK + part * 4]);
+      float mx = fmaxf(fmaxf(sv.x, sv.y), fmaxf(sv.z, sv.w));
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o2));
+      const float m_old = sm.m[h];
+      const float m_new = fmaxf(m_old, mx);
+      const bool none = m_new == -INFINITY;
+      const __half p0 = __float2half_rn(none ? 0.f : exp2f(sv.x - m_new));
+      const __half p1 = __float2half_rn(none ? 0.f : exp2f(sv.y - m_new));
+      const __half p2 = __float2half_rn(none ? 0.f : exp2f(sv.z - m_new));
+      const __half p3 = __float2half_rn(none ? 0.f : exp2f(sv.w - m_new));
+      float sum = __half2float(p0) + __half2float(p1) + __half2float(p2) + __half2float(p3);
+      uint2 pw;
+      pw.x = (uint32_t)__half_as_ushort(p0) | ((uint32_t)__half_as_ushort(p1) << 16);
+      pw.y = (uint32_t)__half_as_ushort(p2) | ((uint32_t)__half_as_ushort(p3) << 16);
+      *reinterpret_cast<uint2*>(&sm.p[h * PS + part * 4]) = pw;
+#pragma unroll
+      for (int o2 = 1; o2 < 16; o2 <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o2);
+      __syncwarp();
+      if (part == 0) {
+        const float al = none ? 1.f : exp2f(m_old - m_new);
+        sm.alpha[h] = al;
+        sm.l[h] = sm.l[h] * al + sum;
+        sm.m[h] = m_new;
+      }
+    }
+    __syncthreads();
+    // ---- O = O * alpha + P V : warp owns channels warp*DW .. +DW
+    {
+      const float al0 = sm.alpha[g], al1 = sm.alpha[g + 8];
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        o[i][0] *= al0; o[i][1] *= al0; o[i][2] *= al1; o[i][3] *= al1;
+      }
+      const uint32_t pa = smem_u32(&sm.p[(lane & 15) * PS + (lane >> 4) * 8]);
+      const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+      for (int kk = 0; kk < kTK / 16; ++kk) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(pa + kk * 32, a0, a1, a2, a3);
+        const uint32_t vb = smem_u32(&sm.k[(kk * 16 + (mi & 1) * 8 + r8) * QS + warp * DW + (mi >> 1) * 8]);
+#pragma unroll
+        for (int np = 0; np < NT / 2; ++np) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + np * 32, b0, b1, b2, b3);
+          mma_f16(o[2 * np], a0, a1, a2, a3, b0, b1);
+          mma_f16(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // ---- normalise and store
+  const float l0 = sm.l[g], l1 = sm.l[g + 8];
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+  const int head0 = hg * kHG + g, head1 = head0 + 8;
+#pragma unroll
+  for (int i = 0; i < NT; ++i) {
+    const int ch = warp * DW + i * 8 + 2 * t4;
+    if (head0 < a.Hq)
+      *reinterpret_cast<float2*>(a.O + (row * a.Hq + head0) * D + ch) = make_float2(o[i][0] * inv0, o[i][1] * inv0);
+    if (head1 < a.Hq)
+      *reinterpret_cast<float2*>(a.O + (row * a.Hq + head1) * D + ch) = make_float2(o[i][2] * inv1, o[i][3] * inv1);
+  }
+  if (a.lse && tid < kHG && hg * kHG + tid < a.Hq) {
+    const float l = sm.l[tid];
+    a.lse[row * a.Hq + hg * kHG + tid] = l > 0.f ? (sm.m[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+  }
+}
+
 // ---- pipelined variant (d = 512) -------------------------------------------------------
 // A ninth warp produces: it resolves the key sources of tile t+1 (indices ->
 // page table -> pool slot, or a window row) and bulk-copies their packed
@@ -636,11 +869,11 @@ static cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s) {
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0) return cudaSuccess;
   if (a.d == 512 && a.K + a.W <= kMaxKeys) {
-    const size_t smem = sizeof(PipeSmem) + (size_t)(a.K + a.W) * sizeof(int64_t);
-    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_pipe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = sizeof(AttnSmem<512>) + (size_t)(a.K + a.W) * sizeof(int64_t);
+    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_rp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((a.Hq + kHG - 1) / kHG, (unsigned)((int64_t)a.B * a.Tq));
-    k_sparse_attn_pipe<<<grid, kPipeThreads, smem, s>>>(a, status_word());
+    k_sparse_attn_rp<<<grid, kAttnThreads, smem, s>>>(a, status_word());
     return counted(cudaGetLastError());
   }
   return launch_attn_d<64>(a, s);
