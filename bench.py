@@ -258,7 +258,7 @@ def time_dominant_kernel(args, g, wl, flush, stream):
     else:              # prefill: attention of the Full layer
         fn = lambda: abi.csa2_sparse_attn(g.dims(), g.cache(), g.window(0), g.Q[0], g.q_pos, g.idx[0],  # noqa
                                           g.cnt[0], 1.0 / math.sqrt(wl.d), g.O[0], g.lse[0])
-        name = "k_sparse_attn"
+        name = "k_sparse_attn_tc"
     fn()
     tot = 0.0
     for k in range(n):
@@ -329,7 +329,7 @@ def roofline(wl, alg, kern, peaks):
     flops = alg["attn_flops"]
     achieved = flops / (kern["ms"] / 1e3) / 1e12
     traffic = committed_traffic(os.path.join(ROOT, "profiles", f"sparse_attn_{wl.name}.md"),
-                                os.path.join(src, "attention.cu"))
+                                os.path.join(src, "attention_tc.cu"))
     return {"bound": "tensor", "kernel": kern["name"], "achieved": achieved, "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
             "algorithmic_flops_per_launch": flops, "kernel_ms": kern["ms"],

@@ -868,6 +868,17 @@ static cudaError_t launch_attn_d(const AttnArgs& a, cudaStream_t s) {
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0) return cudaSuccess;
+  if (sparse_attn_tc_supported(a)) return launch_sparse_attn_tc(a, s);
+  const int64_t ctas = (int64_t)((a.Hq + kHG - 1) / kHG) * a.B * a.Tq;
+  if (a.d == 512 && a.K + a.W <= kMaxKeys && ctas <= 152) {
+    // few CTAs (decode): the producer-warp pipeline hides more latency per CTA
+    const size_t smem = sizeof(PipeSmem) + (size_t)(a.K + a.W) * sizeof(int64_t);
+    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_pipe, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((a.Hq + kHG - 1) / kHG, (unsigned)((int64_t)a.B * a.Tq));
+    k_sparse_attn_pipe<<<grid, kPipeThreads, smem, s>>>(a, status_word());
+    return counted(cudaGetLastError());
+  }
   if (a.d == 512 && a.K + a.W <= kMaxKeys) {
     const size_t smem = sizeof(AttnSmem<512>) + (size_t)(a.K + a.W) * sizeof(int64_t);
     cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_rp, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

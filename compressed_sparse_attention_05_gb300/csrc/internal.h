@@ -144,5 +144,8 @@ struct AttnArgs {
   float* lse;                 // [rows][Hq] or null
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s);
+// ---- attention_tc.cu: tcgen05 kernel for d = 512, Hq <= 64, K + W <= 1024
+bool sparse_attn_tc_supported(const AttnArgs& a);
+cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s);
 
 }  // namespace csa2
