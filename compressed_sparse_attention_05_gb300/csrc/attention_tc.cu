@@ -13,15 +13,19 @@
 //   O^T [512 dims x 64 heads] += V_chunk^T [512 x 128] . P^T    (4 M-tiles x 8 MMAs, k = 16 keys)
 // K = V, so one dequantised shared-memory tile serves as the K-major A
 // operand of the first product and as the MN-major A operand of the second.
-// S^T takes 64 tensor-memory columns, O^T 4 x 64.
+// S^T is accumulated in four interleaved partial sums (4 x 64 tensor-memory
+// columns, summed by the softmax) and O^T in four M-tiles (4 x 64), so that
+// four independent accumulation chains are always in flight: a chain of
+// MMAs into one accumulator waits for each predecessor.
 //
-// A CTA (16 warps) owns one token (all heads) and a contiguous run of its
+// A CTA (16 worker warps and one MMA warp) owns one token (all heads) and a contiguous run of its
 // chunks.  Per chunk: the threads dequantise the tile in four 128-dim slices
-// (thread = one key x 32 dims of every slice); a slice waits only for the
-// previous chunk's PV M-tile that read it, and its eight S MMAs are issued
-// as soon as it is written, so dequantisation overlaps the tensor core.  The
-// next chunk's packed bytes are loaded into registers while the softmax
-// runs.  Softmax (thread = one key x 16 heads): the reference maximum of a
+// (thread = one key x 32 dims of every slice, a warp = 8 whole keys); each
+// warp announces a written slice on an mbarrier and
+// the MMA warp issues the slice's eight S MMAs once all warps have, so
+// dequantisation overlaps the tensor core.  (An MMA issue blocks the issuing
+// thread while the tensor pipe is full, hence a warp of its own.)  A slice's registers are refilled
+// with the next chunk's bytes right after it is stored.  Softmax (thread = one key x 16 heads): the reference maximum of a
 // head only moves when a score exceeds it by more than 2^8 (then O^T is
 // rescaled in tensor memory), so P = exp2(s - m) <= 256 fits fp16 and most
 // chunks need no maximum reduction at all; row sums stay per thread until
@@ -53,7 +57,8 @@ constexpr int kMaxChunks = 8;    // keys per token <= 1,024; also the largest po
 constexpr int kWorkers = 512;             // 16 warps: dequantisation and softmax
 constexpr int kThreads = kWorkers + 32;   // + one warp that allocates tensor memory and issues the MMAs
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 64;
+constexpr uint32_t kColS = 0;     // four partial S^T accumulators (k-step ks goes to ks % 4), 64 columns each
+constexpr uint32_t kColO = 256;   // O^T: four M-tiles of 64 columns
 constexpr float kRescaleLog2 = 8.f;  // move a head's reference maximum only beyond this growth
 
 // Byte offsets inside the operand tiles (no-swizzle canonical layout: core
@@ -181,26 +186,26 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Named barrier / vote among the worker warps only (the MMA warp never joins).
+// Barrier / vote among the worker warps only (the MMA warp never joins).
 __device__ __forceinline__ void workers_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(512) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(kWorkers) : "memory");
 }
 __device__ __forceinline__ bool workers_or(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v), "n"(512)
+      : "r"((uint32_t)v), "n"(kWorkers)
       : "memory");
   return r != 0;
 }
 
-// Packed bytes of one key for the thread's 32 dims (128*sl + 32*qd ..) of
-// each slice sl.  Slice sl lives in v[2sl] (MXFP4: 16 code bytes) or
-// v[2sl], v[2sl+1] (window: 32 codes), so that a slice's registers can be
+// Packed MXFP4 code bytes of one key for the thread's 32 dims (128*sl +
+// 32*qd ..) of each slice sl, in v[sl], so that a slice's registers can be
 // refilled with the next chunk's bytes as soon as the slice is stored.
+// (Window rows, one chunk per token at most, are read when they are stored.)
 struct KeyBytes {
-  uint4 v[8];
+  uint4 v[4];
 };
 // MXFP4 scales of a key: quarter qd loads bytes 8*qd .. +7 (the groups of slice qd)
 __device__ __forceinline__ uint2 load_scales(const AttnArgs& a, int32_t src, int qd) {
@@ -210,13 +215,8 @@ __device__ __forceinline__ uint2 load_scales(const AttnArgs& a, int32_t src, int
 
 template <int SL>
 __device__ __forceinline__ void load_slice(const AttnArgs& a, int32_t src, int qd, KeyBytes& kb) {
-  if (src >= 0) {
-    kb.v[2 * SL] = __ldg(reinterpret_cast<const uint4*>(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL));
-  } else if (src <= -2) {
-    const uint8_t* c = a.swa_codes + (-2 - (int64_t)src) * kD + 32 * qd + 128 * SL;
-    kb.v[2 * SL] = __ldg(reinterpret_cast<const uint4*>(c));
-    kb.v[2 * SL + 1] = __ldg(reinterpret_cast<const uint4*>(c + 16));
-  }
+  if (src >= 0)
+    kb.v[SL] = __ldg(reinterpret_cast<const uint4*>(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL));
 }
 __device__ __forceinline__ float load_wscale(const AttnArgs& a, int32_t src) {
   return src <= -2 ? __ldg(a.swa_scales + (-2 - (int64_t)src)) : 0.f;
@@ -224,15 +224,15 @@ __device__ __forceinline__ float load_wscale(const AttnArgs& a, int32_t src) {
 
 // Dequantise the thread's 32 dims of slice SL into the K tile (4 core-matrix rows).
 template <int SL>
-__device__ __forceinline__ void store_slice(const KeyBytes& kb, uint32_t sc_pair, int32_t src, float wsc, int key,
-                                            int qd, unsigned char* ktile) {
+__device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& kb, uint32_t sc_pair, int32_t src,
+                                            float wsc, int key, int qd, unsigned char* ktile) {
   unsigned char* dst = ktile + (key >> 3) * 8192 + (16 * SL + 4 * qd) * 128 + (key & 7) * 16;
   if (src >= 0) {
     const uint32_t s = e4m3x2_f16x2(sc_pair);
     const uint32_t g0 = prmt(s, s, 0x1010u), g1 = prmt(s, s, 0x3232u);   // (scale, scale) of each group
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint32_t w = word_of(kb.v[2 * SL], j);
+      const uint32_t w = word_of(kb.v[SL], j);
       const uint32_t s2 = j < 2 ? g0 : g1;
       uint4 o;
       o.x = hmul2(e2m1x2_f16x2(w & 0xFFu), s2);   // exact: <= 6 significant bits
@@ -242,9 +242,11 @@ __device__ __forceinline__ void store_slice(const KeyBytes& kb, uint32_t sc_pair
       *reinterpret_cast<uint4*>(dst + j * 128) = o;
     }
   } else if (src <= -2) {
+    const uint8_t* wc = a.swa_codes + (-2 - (int64_t)src) * kD + 32 * qd + 128 * SL;
+    const uint4 cw[2] = {__ldg(reinterpret_cast<const uint4*>(wc)), __ldg(reinterpret_cast<const uint4*>(wc + 16))};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint4 c = kb.v[2 * SL + (j >> 1)];
+      const uint4 c = cw[j >> 1];
       const uint32_t w0 = word_of(c, (j & 1) * 2), w1 = word_of(c, (j & 1) * 2 + 1);
       uint4 o;
       o.x = win2_f16x2(w0 & 0xFFFFu, wsc);
@@ -280,6 +282,27 @@ __device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, in
   return -1;
 }
 
+// Scores of the thread's key for heads 16*hg .. +15, in the log2 domain:
+// the sum of the four partial S^T accumulators times scale*log2(e), or -inf
+// for a missing key.
+__device__ __forceinline__ void load_scores(uint32_t tm, int hg, uint32_t lane_q, bool valid, float sl2,
+                                            float (&x)[16]) {
+  float y[16];
+  tc::tmem_ld16(tm + kColS + 16 * hg + lane_q, x);
+  tc::tmem_ld16(tm + kColS + 64 + 16 * hg + lane_q, y);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] += y[j];
+  tc::tmem_ld16(tm + kColS + 128 + 16 * hg + lane_q, y);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] += y[j];
+  tc::tmem_ld16(tm + kColS + 192 + 16 * hg + lane_q, y);
+  tc::tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = valid ? (x[j] + y[j]) * sl2 : -INFINITY;
+}
+
 // Bounded wait of a whole warp; on time-out the CTA's abort flag is raised.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = false;
@@ -304,7 +327,10 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   const int64_t row = blockIdx.x / n_split;
   const int rank = (int)(blockIdx.x % n_split);
   const int b = (int)(row / a.Tq);
-  const int key = (tid >> 2) & (kChunk - 1), qd = tid & 3;   // dequantisation: one key, 32 dims of each slice
+  // dequantisation: one key, 32 dims of each slice.  A warp holds 8 whole keys
+  // (coalesced loads); lanes 8q .. 8q+7 hold quarter q of the 8 keys, so each
+  // 8-lane phase of a 16-byte store covers 8 distinct bank groups.
+  const int key = ((warp & 15) << 3) | (lane & 7), qd = (lane >> 3) & 3;
   const int q4 = warp & 3, hg = (warp >> 2) & 3;             // softmax: key 32*q4 + lane (= key), heads 16*hg ..
   volatile int* abort = &sm.abort;
 
@@ -396,7 +422,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   const uint32_t tm = sm.tmem;
 
   if (mma_warp) {
-    // ================= MMA issue (one thread) =================
+    // ================= MMA issue (one thread; an MMA issue blocks while the tensor pipe is busy) ====
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_f16(128, kHeads, 0, 0, 0);   // K-major A and B
       constexpr uint32_t kIdO = tc::idesc_f16(128, kHeads, 0, 1, 1);   // MN-major A and B
@@ -413,20 +439,21 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
           tc::tc_fence_after();
 #pragma unroll
           for (int ks = 8 * sl; ks < 8 * sl + 8; ++ks)   // descriptor addresses advance in 16-byte units
-            tc::mma_f16(tm + kColS, dk_s + (uint64_t)(ks * 16), dq_s + (uint64_t)(ks * 16), kIdS, ks > 0);
+            tc::mma_f16(tm + kColS + 64 * (ks & 3), dk_s + (uint64_t)(ks * 16), dq_s + (uint64_t)(ks * 16), kIdS,
+                        ks >= 4);
         }
         if (!ok) { *abort = 1; break; }
         tc::mma_commit(&sm.bar_s);
         if (!tc::mbar_wait(&sm.p_ready, it & 1, 1u << 22)) { *abort = 1; break; }
         tc::tc_fence_after();
 #pragma unroll
-        for (int mt = 0; mt < 4; ++mt) {
+        for (int kk = 0; kk < kChunk / 16; ++kk)
 #pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk)
+          for (int mt = 0; mt < 4; ++mt)   // the four M-tiles are independent chains
             tc::mma_f16(tm + kColO + 64 * mt, dk_o + (uint64_t)(mt * 128 + kk * 1024), dp_o + (uint64_t)(kk * 128),
                         kIdO, (it > 0 || kk > 0) ? 1u : 0u);
-          tc::mma_commit(&sm.bar_pv[mt]);
-        }
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) tc::mma_commit(&sm.bar_pv[mt]);
       }
     }
     __syncwarp();
@@ -442,8 +469,6 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 
     for (int it = 0; it < n_my; ++it) {
       const int32_t nxt_src = it + 1 < n_my ? sm.slot[(it + 1) * kChunk + key] : -1;
-      const uint2 nxt_sc = load_scales(a, nxt_src, qd);
-      const float nxt_wsc = load_wscale(a, nxt_src);
       bool wok = true;
       // ---- dequantise slice by slice; refill each slice's registers with the next chunk
 #define CSA2_SLICE(SL)                                                                   \
@@ -451,10 +476,10 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     if (it > 0) wok = wok && warp_wait(&sm.bar_pv[SL], (it - 1) & 1, abort);             \
     {                                                                                    \
       /* the slice's two group scales were loaded by quarter SL of the key */            \
-      const uint32_t w0 = __shfl_sync(0xffffffffu, cur_sc.x, (lane & ~3) | SL);          \
-      const uint32_t w1 = __shfl_sync(0xffffffffu, cur_sc.y, (lane & ~3) | SL);          \
+      const uint32_t w0 = __shfl_sync(0xffffffffu, cur_sc.x, (lane & 7) | (SL << 3));    \
+      const uint32_t w1 = __shfl_sync(0xffffffffu, cur_sc.y, (lane & 7) | (SL << 3));    \
       const uint32_t pr = ((qd >> 1) ? w1 : w0) >> (16 * (qd & 1));                      \
-      if (wok) store_slice<SL>(kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile);      \
+      if (wok) store_slice<SL>(a, kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile);   \
     }                                                                                    \
     if (it + 1 < n_my) load_slice<SL>(a, nxt_src, qd, kb);                               \
     tc::fence_async_smem();                                                              \
@@ -468,8 +493,8 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 #undef CSA2_SLICE
       const bool valid = sm.slot[it * kChunk + kc] != -1;   // the softmax thread's key
       cur_src = nxt_src;
-      cur_wsc = nxt_wsc;
-      cur_sc = nxt_sc;
+      cur_wsc = load_wscale(a, nxt_src);
+      cur_sc = load_scales(a, nxt_src, qd);
 
       // ---- softmax of the chunk: this thread's key, heads 16*hg .. +15
       wok = wok && warp_wait(&sm.bar_s, it & 1, abort);
@@ -477,19 +502,12 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       float x[16];
       bool above = false;
       if (wok) {
-        tc::tmem_ld16(tm + kColS + 16 * hg + lane_q, x);
-        tc::tmem_wait_ld();
+        load_scores(tm, hg, lane_q, valid, sl2, x);
         const float4* thr = reinterpret_cast<const float4*>(&sm.m_thr[16 * hg]);
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
           const float4 th = thr[j4];
-          const float tj[4] = {th.x, th.y, th.z, th.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = 4 * j4 + u;
-            x[j] = valid ? x[j] * sl2 : -INFINITY;
-            above |= x[j] > tj[u];
-          }
+          above |= (x[4 * j4] > th.x) | (x[4 * j4 + 1] > th.y) | (x[4 * j4 + 2] > th.z) | (x[4 * j4 + 3] > th.w);
         }
       }
       // one vote per chunk: did a score outgrow its head's reference, or has a
@@ -497,12 +515,10 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       const bool seen_abort = *abort != 0;
       if (workers_or(above || seen_abort)) {
         if (workers_or(seen_abort)) break;
-        // reduce the chunk's maxima
-        float t16[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t16[j] = x[j];
-        const float mx = reduce16<true>(t16, lane);
+        // reduce the chunk's maxima (x is consumed, then summed again from tensor memory)
+        const float mx = reduce16<true>(x, lane);
         if (lane < 16) sm.red[q4][16 * hg + lane] = mx;
+        load_scores(tm, hg, lane_q, valid, sl2, x);
         workers_sync();
         int need = 0;
         if (tid < kHeads) {
@@ -639,30 +655,22 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       }
     }
     cluster_sync();
-    // this rank sums heads h0 .. h1 over all ranks: two float4 per thread and
-    // round, every rank's value requested before any is added
+    // this rank sums heads h0 .. h1 over all ranks, every rank's value
+    // requested before any is added
     const int h0 = kHeads * (int)crank / n_split, h1 = kHeads * ((int)crank + 1) / n_split;
     const uint32_t pbase = tc::smem_addr(part);
-    const int e_end = h1 * (kD / 4);
-    for (int e = h0 * (kD / 4) + tid; e < e_end; e += 2 * kThreads) {
-      const int e2 = e + kThreads;
-      float4 r0[kMaxChunks], r1[kMaxChunks];
+    for (int e = h0 * (kD / 4) + tid; e < h1 * (kD / 4); e += kThreads) {
+      float4 r[kMaxChunks];
 #pragma unroll
-      for (int q = 0; q < kMaxChunks; ++q) {
-        r0[q] = q < n_split ? ld_cluster4(map_to_rank(pbase + e * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        r1[q] = (q < n_split && e2 < e_end) ? ld_cluster4(map_to_rank(pbase + e2 * 16, q))
-                                            : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-      float4 s0 = r0[0], s1 = r1[0];
+      for (int q = 0; q < kMaxChunks; ++q)
+        r[q] = q < n_split ? ld_cluster4(map_to_rank(pbase + e * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 s4 = r[0];
 #pragma unroll
       for (int q = 1; q < kMaxChunks; ++q) {
-        s0.x += r0[q].x; s0.y += r0[q].y; s0.z += r0[q].z; s0.w += r0[q].w;
-        s1.x += r1[q].x; s1.y += r1[q].y; s1.z += r1[q].z; s1.w += r1[q].w;
+        s4.x += r[q].x; s4.y += r[q].y; s4.z += r[q].z; s4.w += r[q].w;
       }
-      const int ha = e / (kD / 4), hb2 = e2 / (kD / 4);
-      if (ha < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + ha) * kD + (e % (kD / 4)) * 4) = s0;
-      if (e2 < e_end && hb2 < a.Hq)
-        *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb2) * kD + (e2 % (kD / 4)) * 4) = s1;
+      const int h = e / (kD / 4);
+      if (h < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + h) * kD + (e % (kD / 4)) * 4) = s4;
     }
     cluster_sync();   // no CTA leaves while another still reads its shared memory
   }
