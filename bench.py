@@ -7,7 +7,10 @@ A step is one pass of the layer group over one batch of synthetic input,
 inputs resident in HBM: for the default decode workload (32 sequences x one
 token over a 131,072-token context, Full mode) that is window pack, index
 scoring of every visible entry, Top-512 and sparse attention.  L2 is flushed
-(a 512 MB write) before every timed step.  Under torchrun each rank runs an
+before every timed step: 512 MB are written and then 512 MB of another
+buffer are read, so that no input is resident and the L2 holds clean lines
+(a write alone leaves ~126 MB of dirty lines whose write-back would be
+charged to the first kernels of the step).  Under torchrun each rank runs an
 independent replica on its own GPU (weak scaling, no collective on the data
 path); rank 0 prints the line.
 """
@@ -178,7 +181,7 @@ def run_gpu(args, rank, world, dist):
     wl.seed = replica_seed(wl.seed, rank)
     alg = algorithmic(wl)
     g = harness.LayerGroup(wl, f"cuda:{local}")
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -187,7 +190,7 @@ def run_gpu(args, rank, world, dist):
         torch.cuda.synchronize()
 
     for w in range(args.warmup):
-        flush.fill_(w & 255)
+        flush(w)
         g.step()
     torch.cuda.synchronize()
     assert abi.csa2_get_status() == 0
@@ -198,7 +201,7 @@ def run_gpu(args, rank, world, dist):
     n0 = abi.csa2_launch_count()
     with ClockSampler(local) as clk:
         for k in range(args.steps):
-            flush.fill_(k & 255)
+            flush(k)
             ev[k][0].record(stream)
             g.step()
             ev[k][1].record(stream)
@@ -228,7 +231,7 @@ def run_gpu(args, rank, world, dist):
         "config": {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": tokens,
                    "layers": "".join(wl.layers), "K": wl.K, "Hq": wl.Hq, "d": wl.d, "W": wl.W,
                    "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": "MXFP4 288 B/entry, 64-entry pages",
-                   "l2": "flushed before every timed step (512 MB write)",
+                   "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "step_roofline": step_roofline(wl, alg, ms, peaks),
@@ -241,6 +244,22 @@ def run_gpu(args, rank, world, dist):
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+
+
+class L2Flush:
+    """Evicts the step's inputs from L2: writes FLUSH_BYTES, then reads another
+    FLUSH_BYTES, so that the L2 ends up holding clean lines of neither."""
+
+    def __init__(self, dev):
+        import torch
+        self.device = dev
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(FLUSH_BYTES // 8, dtype=torch.int64, device=dev)
+        self.acc = torch.zeros((), dtype=torch.int64, device=dev)
+
+    def __call__(self, k):
+        self.w.fill_(k & 255)
+        self.acc += self.r.sum()
 
 
 def time_dominant_kernel(args, g, wl, flush, stream):
@@ -262,7 +281,7 @@ def time_dominant_kernel(args, g, wl, flush, stream):
     fn()
     tot = 0.0
     for k in range(n):
-        flush.fill_(k & 255)
+        flush(k)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         fn()
@@ -288,7 +307,7 @@ def time_e2e(args, g, flush, stream, dist):
     if dist is not None:
         dist.barrier()
     for k in range(n):
-        flush.fill_(k & 255)
+        flush(k)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for d_, h in zip(ins, h_in):

@@ -14,9 +14,9 @@
 // K = V, so one dequantised shared-memory tile serves as the K-major A
 // operand of the first product and as the MN-major A operand of the second.
 // S^T is accumulated in four interleaved partial sums (4 x 64 tensor-memory
-// columns, summed by the softmax) and O^T in four M-tiles (4 x 64), so that
-// four independent accumulation chains are always in flight: a chain of
-// MMAs into one accumulator waits for each predecessor.
+// columns, summed by the softmax) and O^T in four M-tiles (4 x 64).  PV runs
+// tile by tile with a commit per tile, so that the next chunk's slice of the
+// K tile is rewritten as soon as the tile that read it is done.
 //
 // A CTA (16 worker warps and one MMA warp) owns one token (all heads) and a contiguous run of its
 // chunks.  Per chunk: the threads dequantise the tile in four 128-dim slices
@@ -447,13 +447,13 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
         if (!tc::mbar_wait(&sm.p_ready, it & 1, 1u << 22)) { *abort = 1; break; }
         tc::tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kChunk / 16; ++kk)
+        for (int mt = 0; mt < 4; ++mt) {   // tile by tile: a finished tile frees its K slice for the next chunk
 #pragma unroll
-          for (int mt = 0; mt < 4; ++mt)   // the four M-tiles are independent chains
+          for (int kk = 0; kk < kChunk / 16; ++kk)
             tc::mma_f16(tm + kColO + 64 * mt, dk_o + (uint64_t)(mt * 128 + kk * 1024), dp_o + (uint64_t)(kk * 128),
                         kIdO, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int mt = 0; mt < 4; ++mt) tc::mma_commit(&sm.bar_pv[mt]);
+          tc::mma_commit(&sm.bar_pv[mt]);
+        }
       }
     }
     __syncwarp();

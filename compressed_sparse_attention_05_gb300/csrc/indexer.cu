@@ -224,24 +224,43 @@ __device__ __forceinline__ int row_pages(const IndexerArgs& a, int b) {
 // Balanced single-wave partition when every row has one query (Tq == 1):
 // with P pages in all and S CTA slots, every row gets ceil(pages_b / ppc)
 // CTAs of ppc = ceil(P / (S - B)) pages, so the grid never exceeds S and no
-// CTA spans two rows.  Each CTA derives its (row, page range) itself.
+// CTA spans two rows.  Each CTA derives its (row, page range) itself; every
+// warp computes it with its lanes on 32 rows at a time (warp sums and a
+// prefix scan), so the set-up costs one round of loads, not one per row.
 __device__ __forceinline__ bool flat_assign(const IndexerArgs& a, int slots, int& b_out, int& p0, int& p1) {
+  const int lane = threadIdx.x & 31;
   int64_t total = 0;
-  for (int b = 0; b < a.B; ++b) total += row_pages(a, b);
+  for (int base = 0; base < a.B; base += 32) {
+    const int b = base + lane;
+    int pb = b < a.B ? row_pages(a, b) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pb += __shfl_xor_sync(0xffffffffu, pb, o);
+    total += pb;
+  }
   const int denom = max(1, slots - a.B);
   int64_t ppc64 = (total + denom - 1) / denom;
   const int ppc = ppc64 < 1 ? 1 : (int)ppc64;
   int c = blockIdx.x;
-  for (int b = 0; b < a.B; ++b) {
-    const int pb = row_pages(a, b);
+  for (int base = 0; base < a.B; base += 32) {
+    const int b = base + lane;
+    const int pb = b < a.B ? row_pages(a, b) : 0;
     const int nc = (pb + ppc - 1) / ppc;
-    if (c < nc) {
-      b_out = b;
-      p0 = c * ppc;
-      p1 = min(pb, p0 + ppc);
+    int incl = nc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = incl - nc;
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (c < tot) {
+      const int owner = __ffs(__ballot_sync(0xffffffffu, c >= excl && c < incl)) - 1;
+      b_out = base + owner;
+      p0 = (c - __shfl_sync(0xffffffffu, excl, owner)) * ppc;
+      p1 = min(__shfl_sync(0xffffffffu, pb, owner), p0 + ppc);
       return p0 < p1;
     }
-    c -= nc;
+    c -= tot;
   }
   return false;
 }
@@ -288,15 +307,26 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
   volatile int* abort = &ss.abort;
 
   if (warp == kScanConsumers) {
-    // ---- producer
-    if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < n_pages; ++i) {
-        const int st = i % kScanStages;
-        if (i >= kScanStages && !scan_wait(&ss.empty[st], ((i / kScanStages) - 1) & 1, abort)) break;
-        const int lp = p0 + i;
-        const int pg = lp < a.max_pages ? a.page_table[(int64_t)b * a.max_pages + lp] : -1;
-        if (pg < 0 || pg >= a.n_pages) {
+    // ---- producer warp: the page ids come 32 at a time, one batch ahead, so
+    // that no page copy waits for its page-table read; lane 0 issues the copies
+    const int64_t pt_row = (int64_t)b * a.max_pages;
+    auto page_id = [&](int lp) -> int {
+      return (lp < p1 && lp < a.max_pages) ? __ldg(a.page_table + pt_row + lp) : -1;
+    };
+    int cur = page_id(p0 + lane), nxt = page_id(p0 + 32 + lane);
+    int issued = 0;
+    for (int i = 0; i < n_pages; ++i) {
+      if (i > 0 && (i & 31) == 0) {
+        cur = nxt;
+        nxt = page_id(p0 + i + 32 + lane);
+      }
+      const int pg = __shfl_sync(0xffffffffu, cur, i & 31);
+      const int st = i % kScanStages;
+      bool ok = true;
+      if (lane == 0) {
+        if (i >= kScanStages && !scan_wait(&ss.empty[st], ((i / kScanStages) - 1) & 1, abort)) {
+          ok = false;
+        } else if (pg < 0 || pg >= a.n_pages) {
           raise_status(status, CSA2_STATUS_BAD_PAGE);
           ss.valid[st] = 0;
           tc::mbar_arrive(&ss.full[st]);
@@ -307,15 +337,17 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
                        reinterpret_cast<const unsigned char*>(a.k) + (int64_t)pg * kPageBytes, kPageBytes,
                        &ss.full[st]);
         }
-        issued = i + 1;
       }
-      // drain: every issued copy must have landed before the CTA exits
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      issued = i + 1;
+    }
+    // drain: every issued copy must have landed before the CTA exits
+    if (lane == 0)
       for (int i = max(0, issued - kScanStages); i < issued; ++i) {
         const int st = i % kScanStages;
         for (uint32_t k = 0; k < (1u << 22); ++k)
           if (tc::mbar_try_wait(&ss.full[st], (i / kScanStages) & 1)) break;
       }
-    }
   } else {
     // ---- consumers: warp w owns entries 16w .. 16w+15 of every page
     const int g = lane >> 2, t = lane & 3;
