@@ -397,17 +397,19 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   IndexerArgs a = indexer_args(dm, c, idx_q, w, q_pos);
   a.max_entries = max_entries;
   if (!reindex) {
-    LAUNCH(cudaMemsetAsync(hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
+    // the many-query GEMM path builds no histogram: the Top-K kernel then builds each row's
+    if (index_scores_gemm_supported(a)) hist = nullptr;
+    if (hist) LAUNCH(cudaMemsetAsync(hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
     LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s),
            "index_scores");
     ValidSpec v{nullptr, c->n_entries, q_pos, dm->Tq, 1, max_entries};
-    if (rows <= kSplitTopkMaxRows && max_entries >= kSplitTopkMinEntries)
+    if (hist && rows <= kSplitTopkMaxRows && max_entries >= kSplitTopkMinEntries)
       LAUNCH(launch_topk_split(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist,
                                kHistBins, base + L.split_off, s),
              "topk");
     else
-      LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins,
-                         s),
+      LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist,
+                         hist ? kHistBins : 0, s),
              "topk");
     if (out_pool) {
       ValidSpec vb{nullptr, c->n_entries, q_pos, dm->Tq, 8, max_entries};

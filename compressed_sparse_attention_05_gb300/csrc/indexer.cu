@@ -624,6 +624,13 @@ static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, co
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
                                 int64_t bm_stride, int block, int max_entries, uint32_t* hist, cudaStream_t s) {
   if ((int64_t)a.B * a.Tq == 0 || max_entries == 0) return cudaSuccess;
+  if (block == 8 && index_scores_gemm_supported(a)) {
+    cudaError_t e = launch_index_scores_gemm(a, scores, stride, blockmax, bm_stride, max_entries, s);
+    if (e != cudaSuccess || !hist) return e;
+    dim3 hg((max_entries + 255) / 256, a.B * a.Tq);
+    k_score_hist<<<hg, 256, 0, s>>>(scores, stride, a, hist);
+    return counted(cudaGetLastError());
+  }
   if (mma_path(a) && block == 8 && a.Di == 128) {
     if (a.Hi > 8) return launch_scan_pages<2>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
     return launch_scan_pages<1>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);

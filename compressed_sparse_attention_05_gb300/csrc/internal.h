@@ -79,6 +79,12 @@ struct IndexerArgs {
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride,
                                 float* blockmax, int64_t bm_stride, int block, int max_entries,
                                 uint32_t* hist, cudaStream_t s);
+// ---- indexer_tc.cu: many query tokens per sequence (prefill) as a tcgen05 GEMM
+// (bf16 keys, Hi = 8, Di = 128, Tq >= 32).  Scores and block maxima as above;
+// builds no histogram (the Top-K kernel builds its own).
+bool index_scores_gemm_supported(const IndexerArgs& a);
+cudaError_t launch_index_scores_gemm(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
+                                     int64_t bm_stride, int max_entries, cudaStream_t s);
 // Reindex: compact scores[row][p*block + e] of the pooled blocks' visible
 // positions; n_valid[row] receives the compact count.
 cudaError_t launch_index_scores_pool(const IndexerArgs& a, const int32_t* pool,

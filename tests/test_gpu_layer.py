@@ -150,6 +150,36 @@ def test_index_scores_tolerance():
         assert np.array_equal(bm[b, :len(ref_bm)].cpu().double().numpy(), ref_bm)
 
 
+def test_index_scores_many_queries():
+    """Many query tokens per sequence (the tensor-core GEMM path): 80 tokens are
+    two full 32-token blocks and a ragged one; every visible score of every
+    token against the oracle on the keys as stored, block maxima exact."""
+    wl = WL.prefill_64k(n_new=80, ctx=4096 + 80, H=256)
+    g = harness.LayerGroup(wl)
+    g.step()
+    torch.cuda.synchronize()
+    stride = g.max_entries
+    rows = wl.B * wl.Tq
+    scores = torch.full((rows, stride), float("nan"), device="cuda")
+    bm = torch.full((rows, (stride + 7) // 8), float("nan"), device="cuda")
+    abi.csa2_index_scores(g.dims(), g.cache(), g.idx_q[0], g.idx_w[0], g.q_pos, scores, bm)
+    torch.cuda.synchronize()
+    assert abi.csa2_get_status() == 0
+    n_ent = wl.entries_after(0)
+    ids = torch.arange(n_ent)
+    slots = g.page_table[0, ids // 64].long().cpu() * 64 + ids % 64
+    K = g.idx_k[slots.cuda()].float().cpu().double().numpy()
+    qpos = wl.q_pos()
+    for i in range(wl.Tq):
+        nv = I.n_visible(n_ent, int(qpos[0, i]))
+        q, w = _np(wl.idx_q_row(0, 0, i)), _np(wl.idx_w_row(0, 0, i))
+        s_ref = I.index_scores(q, w, K[:nv])
+        s_gpu = scores[i, :nv].cpu().numpy()
+        assert parity.score_err(s_gpu, s_ref, I.score_condition(q, w, K[:nv])) <= parity.SCORE_RTOL, f"token {i}"
+        ref_bm = I.block_scores(s_gpu, 8)
+        assert np.array_equal(bm[i, :len(ref_bm)].cpu().double().numpy(), ref_bm), f"token {i}"
+
+
 # ---- full-size workloads, sampled ------------------------------------------------------
 
 def test_full_decode_128k_b32():
