@@ -38,36 +38,54 @@ FLUSH_BYTES = 512 << 20
 # workload bytes / flops (algorithmic: what the method must move or compute)
 
 def algorithmic(wl):
-    """Per-step algorithmic work of the workload's hot path and its dominant kernel."""
+    """Per-step algorithmic work of the workload's hot path: unique HBM bytes and FLOPs.
+
+    Bytes count what a step must move at least once: each sequence's visible
+    indexer keys per Full layer (all query tokens of a sequence share them),
+    the pooled keys per Reindex query, the selected MXFP4 entries (at most the
+    entries that exist), the queries read, the outputs written and the index
+    scores written and read back once, plus the hidden states of a prefill
+    chunk.  For one query token per sequence this is the per-query sum.
+    """
     d, Di, K, W, Hq = wl.d, wl.Di, wl.K, wl.W, wl.Hq
     entry_bytes = d // 2 + d // 16                       # 288 B MXFP4 entry (d = 512)
     idx_elt = 2 if wl.idx_dtype == "bf16" else 4
-    scan = 0          # indexer keys read by Full layers
+    scan = 0          # indexer keys read by Full layers (unique per sequence)
     pooled = 0        # indexer keys read by Reindex layers
-    gathered = 0      # selected MXFP4 entries gathered by attention
+    gathered = 0      # selected MXFP4 entries gathered by attention (unique bound)
+    io = 0            # queries, outputs, index scores
     attn_flops = 0
     idx_flops = 0
     for b in range(wl.B):
-        for i in range(wl.Tq):
-            t = wl.t_first[b] + i
-            nv = max(0, min(wl.entries_after(b), (t + 1) // 4))
-            nk = min(K, nv)
-            nwin = min(W, t + 1)
-            for mode in wl.layers:
+        n_ent = wl.entries_after(b)
+        nvs = [max(0, min(n_ent, (wl.t_first[b] + i + 1) // 4)) for i in range(wl.Tq)]
+        for mode in wl.layers:
+            if mode == "F":
+                scan += max(nvs) * Di * idx_elt
+            sel = 0
+            for i in range(wl.Tq):
+                t = wl.t_first[b] + i
+                nv = nvs[i]
+                nk = min(K, nv)
+                nwin = min(W, t + 1)
+                sel += nk
                 if mode == "F":
-                    scan += nv * Di * idx_elt
                     idx_flops += 2 * nv * wl.Hi * Di
+                    io += 2 * nv * 4                     # score written, read back by the Top-K
                 elif mode == "X":
                     npos = min(nv, wl.pool_blocks * wl.pool_block)
                     pooled += npos * Di * idx_elt
                     idx_flops += 2 * npos * wl.Hi * Di
-                gathered += nk * entry_bytes
+                    io += 2 * npos * 4
                 attn_flops += 4 * Hq * d * (nk + nwin)
+            gathered += min(sel, n_ent) * entry_bytes
+            io += wl.Tq * Hq * d * (2 + 4)                # Q (bf16) in, O (fp32) out
     compress_flops = 0
     if wl.H is not None:
         compress_flops = 2 * sum(wl.new_entries(b) for b in range(wl.B)) * 4 * wl.H * (d + Di)
-    return {"scan_bytes": scan, "pooled_bytes": pooled, "gathered_bytes": gathered,
-            "step_bytes": scan + pooled + gathered, "attn_flops": attn_flops, "index_flops": idx_flops,
+        io += wl.B * wl.Tq * wl.H * 2                     # hidden states (bf16)
+    return {"scan_bytes": scan, "pooled_bytes": pooled, "gathered_bytes": gathered, "io_bytes": io,
+            "step_bytes": scan + pooled + gathered + io, "attn_flops": attn_flops, "index_flops": idx_flops,
             "compress_flops": compress_flops}
 
 

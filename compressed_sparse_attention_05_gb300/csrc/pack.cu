@@ -108,6 +108,10 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
                  uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
                  int Di, int idx_dtype, void* idx_k, uint32_t* status) {
   __shared__ float row_buf[kNrpWarps][512];
+  __shared__ double inv_freq[256];   // base^(-2i/r), i < r/2 (r <= 512)
+  // the r/2 rotation frequencies once per CTA, in fp64
+  for (int i = threadIdx.x; i < r / 2; i += blockDim.x) inv_freq[i] = pow((double)rope_base, -2.0 * (double)i / (double)r);
+  __syncthreads();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
   if (m >= (int64_t)B * n_max) return;
@@ -156,9 +160,12 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
       if (ch < d - r) continue;
       const bool first = ch < d - half;
       const int pi = first ? ch - (d - r) : ch - (d - half);
-      const double inv_freq = pow((double)rope_base, -2.0 * (double)pi / (double)r);
+      // angle reduced to [-pi, pi] in fp64 first (positions reach 4M, so the
+      // angle can be ~4e6 rad); sincos then stays on its short path
+      const double ang = pos * inv_freq[pi];
+      const double red = fma(-6.283185307179586, rint(ang * 0.15915494309189535), ang);
       double sn, cs;
-      sincos(pos * inv_freq, &sn, &cs);
+      sincos(red, &sn, &cs);
       const double self = (double)row_buf[warp][ch];
       if (first) {
         const double other = (double)row_buf[warp][ch + half];
