@@ -13,7 +13,7 @@ import numpy as np
 
 SCORE_RTOL = 1e-5
 ATTN_RTOL = 3e-3
-LSE_ATOL = 1e-3   # softmax normaliser summed from fp16-rounded weights (relative error <= 2^-11)
+LSE_ATOL = 1e-3   # normaliser summed from fp32 or fp16-rounded P: relative difference <= 2^-11
 
 
 def score_err(s_gpu, s_ref, cond):

@@ -78,8 +78,8 @@ def check_group(wl, samples, group=None):
             O, lse = A.sparse_attention(Q, st.kv_rows(gi[:gc]), st.swa_rows(l, A.window_positions(t, wl.W)), tau)
             err = parity.attn_err(g.O[l][b, i].cpu().numpy(), O)
             assert err <= parity.ATTN_RTOL, f"layer {l} ({mode}) token {(b, i)}: attention error {err}"
-            # lse = log of the softmax normaliser, summed from the fp16-rounded weights
-            # the PV product uses (relative rounding <= 2^-11 per weight)
+            # lse = log of the softmax normaliser; the kernels sum it from the fp32 or
+            # the fp16-rounded weights (relative difference <= 2^-11 per weight)
             assert np.allclose(g.lse[l][b, i].cpu().numpy(), lse, rtol=0, atol=parity.LSE_ATOL)
     return g, swaps
 
