@@ -157,9 +157,7 @@ k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t st
         if (hist) {
           // lanes t == 0 carry entry g, lanes t == 1 entry g + 8
           const bool has = (t == 0 && vg) || (t == 1 && vg8);
-          const uint32_t bin = has ? score_key(t == 0 ? sg : sg8) >> 21 : 0xFFFFFFFFu;
-          const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-          if (has && lane == __ffs(peers) - 1) atomicAdd(&shist[(i - i0) * kHistBins + bin], __popc(peers));
+          if (has) atomicAdd(&shist[(i - i0) * kHistBins + (score_key(t == 0 ? sg : sg8) >> 21)], 1u);
         }
         if (blockmax) {
           float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;
@@ -390,9 +388,7 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
           if (t == 1 && vg8) scores[row * stride + e0 + g + 8] = sg8;
           if (hist) {
             const bool has = (t == 0 && vg) || (t == 1 && vg8);
-            const uint32_t bin = has ? score_key(t == 0 ? sg : sg8) >> 21 : 0xFFFFFFFFu;
-            const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-            if (has && lane == __ffs(peers) - 1) atomicAdd(&shist[(qi - i0) * kHistBins + bin], __popc(peers));
+            if (has) atomicAdd(&shist[(qi - i0) * kHistBins + (score_key(t == 0 ? sg : sg8) >> 21)], 1u);
           }
           if (blockmax) {
             float m0 = vg ? sg : -INFINITY, m1 = vg8 ? sg8 : -INFINITY;

@@ -84,11 +84,11 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
   return block_exclusive_scan_t<kTopkThreads>(v, warp_tot);
 }
 
-// Adds `digit` (< nbins, or >= nbins for "none") to a shared histogram with
-// one atomic per distinct digit of the warp.
+// Adds `digit` (< nbins, or >= nbins for "none") to a shared histogram: one
+// shared atomic per lane (match.any aggregation costs more than the rare
+// serialisation of equal digits).
 __device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, uint32_t nbins) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-  if (digit < nbins && (threadIdx.x & 31) == (uint32_t)(__ffs(peers) - 1)) atomicAdd(&hist[digit], __popc(peers));
+  if (digit < nbins) atomicAdd(&hist[digit], 1u);
 }
 
 // Slot in a shared list for every lane with `take` (one atomic per warp); -1
