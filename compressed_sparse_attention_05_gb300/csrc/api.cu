@@ -123,11 +123,17 @@ static IndexerArgs indexer_args(const csa2_dims* dm, const csa2_cache* c, const 
 // Workspace of csa2_index_topk: scores, block maxima, valid counts.
 constexpr int kHistBins = 2048;  // score-key histogram bins per row (top 11 key bits)
 
-// Few, long rows take the split Top-K (many CTAs per row): measured on the
-// 1M-context group (8 rows of 262,144 entries) it saves ~30 us per step, on
-// 32 rows of 32,768 entries the single-CTA rows are faster.
+// Long rows take the split Top-K (many CTAs per row): measured on the
+// 1M-context group (8 rows of 262,144 entries) it saves ~30 us per step; on
+// 32 rows of 32,768 entries the single-CTA rows are faster.  A batch whose
+// longest row reaches 2^17 entries splits whatever its row count (one CTA per
+// row would leave that row's scan of ~128K+ scores on one SM).
 constexpr int64_t kSplitTopkMaxRows = 16;
 constexpr int kSplitTopkMinEntries = 1 << 16;
+constexpr int kSplitTopkAlwaysEntries = 1 << 17;
+static bool use_split_topk(int64_t rows, int32_t max_entries) {
+  return (rows <= kSplitTopkMaxRows && max_entries >= kSplitTopkMinEntries) || max_entries >= kSplitTopkAlwaysEntries;
+}
 
 struct IndexWs {
   size_t scores_off, bm_off, nvalid_off, hist_off, split_off, total;
@@ -147,8 +153,7 @@ static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
   L.nvalid_off = round_up(L.bm_off + (size_t)(rows * L.bm_stride) * 4, 256);
   L.hist_off = round_up(L.nvalid_off + (size_t)rows * 4, 256);
   L.split_off = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
-  const size_t split = (rows <= kSplitTopkMaxRows && max_entries >= kSplitTopkMinEntries)
-                           ? topk_split_scratch_bytes(rows, L.s_stride) : 0;
+  const size_t split = use_split_topk(rows, max_entries) ? topk_split_scratch_bytes(rows, L.s_stride) : 0;
   L.total = round_up(L.split_off + split, 256);
   return L;
 }
@@ -403,7 +408,7 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
     LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s),
            "index_scores");
     ValidSpec v{nullptr, c->n_entries, q_pos, dm->Tq, 1, max_entries};
-    if (hist && rows <= kSplitTopkMaxRows && max_entries >= kSplitTopkMinEntries)
+    if (hist && use_split_topk(rows, max_entries))
       LAUNCH(launch_topk_split(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist,
                                kHistBins, base + L.split_off, s),
              "topk");

@@ -334,10 +334,11 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   const int q4 = warp & 3, hg = (warp >> 2) & 3;             // softmax: key 32*q4 + lane (= key), heads 16*hg ..
   volatile int* abort = &sm.abort;
 
-  // ---- round 1 of loads (all independent): the token's scalars and its Q rows
+  pdl_trigger();
+  // ---- before the previous kernel of the step is done: the token's own inputs
+  // (scalars, Q rows), barriers, tensor memory and the Q operand
   const int t = a.q_pos[row];
   const int n_ent = a.n_entries[b];
-  int n_sel = a.cnt[row];
   const int pos0 = a.swa_cap > 0 ? a.swa_pos0[b] : 0;
   uint4 qv[8];   // unit = (head, 8 dims); 8 heads of a unit group share a core matrix
 #pragma unroll
@@ -346,30 +347,6 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     const int h = ((u >> 9) << 3) | (u & 7), c8 = (u >> 3) & 63;
     qv[r] = (!mma_warp && h < a.Hq) ? __ldg(reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + h) * kD + c8 * 8))
                                     : make_uint4(0, 0, 0, 0);
-  }
-  // the key list: selected entries, then window rows
-  const int nv = n_visible(n_ent, t);
-  if (n_sel < 0 || n_sel > a.K) {
-    if (tid == 0 && rank == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
-    n_sel = n_sel < 0 ? 0 : a.K;
-  }
-  const int w_lo = max(max(0, t - a.W + 1), pos0);
-  const int w_hi = min(t, pos0 + a.swa_cap - 1);
-  const int n_win = max(0, w_hi - w_lo + 1);
-  const int n_keys = n_sel + n_win;
-  const int n_chunks = (n_keys + kChunk - 1) / kChunk;   // <= kMaxChunks (checked by the launcher)
-  const int c0 = n_chunks * rank / n_split, c1 = n_chunks * (rank + 1) / n_split;
-  const int n_my = c1 - c0;
-
-  // ---- rounds 2-3: key sources.  Every worker resolves its key in the first
-  // chunk; the key's later chunks are shared out among its four threads.
-  int32_t cur_src = -1;
-  if (!mma_warp && n_my > 0) {
-    cur_src = key_source(a, row, b, c0 * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, qd == 0, status);
-    if (qd == 0) sm.slot[key] = cur_src;
-    for (int c = qd + 1; c < n_my; c += 4)
-      sm.slot[c * kChunk + key] =
-          key_source(a, row, b, (c0 + c) * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, true, status);
   }
   if (tid == 0) {
     tc::mbar_init(&sm.bar_s, 1);
@@ -402,6 +379,33 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(sm.q) + (h >> 3) * 8192 + c8 * 128 + (h & 7) * 16) =
           make_uint4(ov[0], ov[1], ov[2], ov[3]);
     }
+  }
+  // ---- the selection (and the window rows) come from earlier kernels of the step
+  pdl_wait();
+  int n_sel = a.cnt[row];
+  const int nv = n_visible(n_ent, t);
+  if (n_sel < 0 || n_sel > a.K) {
+    if (tid == 0 && rank == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    n_sel = n_sel < 0 ? 0 : a.K;
+  }
+  // the key list: selected entries, then window rows
+  const int w_lo = max(max(0, t - a.W + 1), pos0);
+  const int w_hi = min(t, pos0 + a.swa_cap - 1);
+  const int n_win = max(0, w_hi - w_lo + 1);
+  const int n_keys = n_sel + n_win;
+  const int n_chunks = (n_keys + kChunk - 1) / kChunk;   // <= kMaxChunks (checked by the launcher)
+  const int c0 = n_chunks * rank / n_split, c1 = n_chunks * (rank + 1) / n_split;
+  const int n_my = c1 - c0;
+
+  // ---- key sources.  Every worker resolves its key in the first chunk; the
+  // key's later chunks are shared out among its four threads.
+  int32_t cur_src = -1;
+  if (!mma_warp && n_my > 0) {
+    cur_src = key_source(a, row, b, c0 * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, qd == 0, status);
+    if (qd == 0) sm.slot[key] = cur_src;
+    for (int c = qd + 1; c < n_my; c += 4)
+      sm.slot[c * kChunk + key] =
+          key_source(a, row, b, (c0 + c) * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, true, status);
   }
   // ---- round 4: the first chunk's packed bytes
   float cur_wsc = 0.f;
@@ -707,13 +711,15 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)n_split;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_trigger / pdl_wait
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)n_split;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = n_split > 1 ? 1 : 0;
+  cfg.numAttrs = n_split > 1 ? 2 : 1;
   return counted(cudaLaunchKernelEx(&cfg, k_sparse_attn_tc, a, status_word(), n_split));
 }
 

@@ -112,6 +112,15 @@ __device__ __forceinline__ int n_visible(int n_entries, int t) {
   return v < n_entries ? v : n_entries;
 }
 
+// Programmatic dependent launch: the kernels of a layer step are launched so
+// that the next one may start its independent prologue while this one runs.
+// pdl_trigger lets the next kernel launch; pdl_wait blocks until the previous
+// kernel has completed and its writes are visible (a no-op when the launch
+// carried no dependency).  Every kernel launched with launch_step calls
+// pdl_wait before it reads anything an earlier kernel of the step wrote.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void raise_status(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
 }

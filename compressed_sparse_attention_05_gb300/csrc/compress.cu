@@ -155,6 +155,8 @@ k_compress_gemm_tc(const uint16_t* __restrict__ hidden, int G, int T, int H, con
   __shared__ uint64_t bar_free[kTcStages];
   __shared__ uint64_t bar_done;
   __shared__ uint32_t tmem_slot;
+  pdl_trigger();
+  pdl_wait();
   const uint32_t pad = (1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u;
   unsigned char* ring = smem_raw + pad;
   const int N = d + Di;
@@ -291,9 +293,8 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
     const size_t smem = kTcStages * kTcStageBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_compress_gemm_tc<<<grid, kTcThreads, smem, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M,
-                                                      Kd / n_split, partials, status_word());
-    return counted(cudaGetLastError());
+    return launch_step(k_compress_gemm_tc, grid, dim3(kTcThreads), smem, s, hidden, G, T, H, W, d, W_idx,
+                       W_idx ? Di : 0, M, Kd / n_split, partials, status_word());
   }
   k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M,
                                              Kd / n_split, partials);

@@ -270,6 +270,8 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
                    uint32_t* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ ScanShared ss;
+  pdl_trigger();
+  pdl_wait();
   unsigned char* ring = smem_raw;                                   // kScanStages pages
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem_raw + kScanStages * kPageBytes);
   int b, p0, p1, i0, i1;
@@ -448,14 +450,12 @@ static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_
     if (e != cudaSuccess || per_sm < 1) per_sm = 1;
     const int slots = per_sm * num_sms();
     const int grid = slots > a.B ? slots : a.B + 1;
-    k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, 1, 0, grid, scores, stride, blockmax, bm_stride,
-                                                             hist, status_word());
-    return counted(cudaGetLastError());
+    return launch_step(k_index_scan_pages<NT>, dim3(grid), dim3(kScanThreads), smem, s, a, 1, 0, grid, scores, stride,
+                       blockmax, bm_stride, hist, status_word());
   }
   dim3 grid((max_pages_vis + ppc - 1) / ppc, q_groups, a.B);
-  k_index_scan_pages<NT><<<grid, kScanThreads, smem, s>>>(a, QG, ppc, 0, scores, stride, blockmax, bm_stride, hist,
-                                                          status_word());
-  return counted(cudaGetLastError());
+  return launch_step(k_index_scan_pages<NT>, grid, dim3(kScanThreads), smem, s, a, QG, ppc, 0, scores, stride,
+                     blockmax, bm_stride, hist, status_word());
 }
 
 // Histogram of already-written scores (the generic scoring path).
@@ -480,6 +480,8 @@ k_index_scores_pool_mma(IndexerArgs a, const int32_t* __restrict__ pool,
                         const int32_t* __restrict__ pool_cnt, int n_pool,
                         float* __restrict__ scores, int64_t stride, int32_t* __restrict__ n_valid,
                         uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.y;
   const int b = (int)(row / a.Tq);
   const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[row]);
@@ -604,9 +606,8 @@ static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, co
                                    cudaStream_t s) {
   const int pairs = (n_pool + 1) / 2;
   dim3 grid((pairs + kIdxWarps - 1) / kIdxWarps, a.B * a.Tq);
-  k_index_scores_pool_mma<NCH, NT><<<grid, kIdxWarps * 32, 0, s>>>(a, pool, pool_cnt, n_pool, scores,
-                                                                   stride, n_valid, status_word());
-  return counted(cudaGetLastError());
+  return launch_step(k_index_scores_pool_mma<NCH, NT>, grid, dim3(kIdxWarps * 32), 0, s, a, pool, pool_cnt, n_pool,
+                     scores, stride, n_valid, status_word());
 }
 
 #define CSA2_DISPATCH_MMA(FN, ...)                                  \

@@ -71,6 +71,8 @@ k_index_scores_gemm(IndexerArgs a, const __grid_constant__ CUtensorMap kmap, int
                     float* __restrict__ scores, int64_t stride, float* __restrict__ blockmax, int64_t bm_stride,
                     uint32_t* status) {
   extern __shared__ unsigned char smem_raw[];
+  pdl_trigger();
+  pdl_wait();
   const uint32_t pad = (1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u;
   GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw + pad);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -291,9 +293,8 @@ cudaError_t launch_index_scores_gemm(const IndexerArgs& a, float* scores, int64_
   e = cudaFuncSetAttribute(k_index_scores_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(splits, q_blocks, a.B);
-  k_index_scores_gemm<<<grid, kGThreads, smem, s>>>(a, map, tiles_per_cta, scores, stride, blockmax, bm_stride,
-                                                     status_word());
-  return counted(cudaGetLastError());
+  return launch_step(k_index_scores_gemm, grid, dim3(kGThreads), smem, s, a, map, tiles_per_cta, scores, stride,
+                     blockmax, bm_stride, status_word());
 }
 
 }  // namespace csa2

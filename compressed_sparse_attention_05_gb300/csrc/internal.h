@@ -24,6 +24,24 @@ uint32_t* status_word();
 // Counts one kernel launch (csa2_launch_count) and returns the launch status.
 cudaError_t counted(cudaError_t launch_status);
 
+// Launches a step kernel with programmatic stream serialisation (see
+// pdl_trigger / pdl_wait in common.cuh) and counts it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_step(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                        Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
+}
+
 // ---- pack.cu ----------------------------------------------------------------
 cudaError_t launch_pack_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* codes,
                               uint8_t* scales, cudaStream_t s);

@@ -84,6 +84,8 @@ __global__ void k_pack_fp8_window(const float* __restrict__ x, int B, int Tq, in
                                   const int32_t* __restrict__ q_pos, const int32_t* __restrict__ pos0,
                                   int swa_cap, uint8_t* __restrict__ codes,
                                   float* __restrict__ scales, uint32_t* status) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (row >= (int64_t)B * Tq) return;
   const int b = (int)(row / Tq);
@@ -110,8 +112,10 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
   __shared__ float row_buf[kNrpWarps][512];
   __shared__ double inv_freq[256];   // base^(-2i/r), i < r/2 (r <= 512)
   // the r/2 rotation frequencies once per CTA, in fp64
+  pdl_trigger();
   for (int i = threadIdx.x; i < r / 2; i += blockDim.x) inv_freq[i] = pow((double)rope_base, -2.0 * (double)i / (double)r);
   __syncthreads();
+  pdl_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
   if (m >= (int64_t)B * n_max) return;
@@ -227,9 +231,8 @@ cudaError_t launch_pack_fp8_window(const float* x, int B, int Tq, int d, const i
                                    float* scales, cudaStream_t s) {
   const int64_t rows = (int64_t)B * Tq;
   if (rows == 0) return cudaSuccess;
-  k_pack_fp8_window<<<grid_for(rows, 8), 256, 0, s>>>(x, B, Tq, d, q_pos, pos0, swa_cap, codes,
-                                                      scales, status_word());
-  return counted(cudaGetLastError());
+  return launch_step(k_pack_fp8_window, dim3(grid_for(rows, 8)), dim3(256), 0, s, x, B, Tq, d, q_pos, pos0, swa_cap,
+                     codes, scales, status_word());
 }
 
 cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r,
@@ -241,10 +244,9 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
                                   cudaStream_t s) {
   const int64_t rows = (int64_t)B * n_max;
   if (rows == 0) return cudaSuccess;
-  k_norm_rope_pack<<<grid_for(rows, kNrpWarps), kNrpWarps * 32, 0, s>>>(
+  return launch_step(k_norm_rope_pack, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
       src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
       n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, status_word());
-  return counted(cudaGetLastError());
 }
 
 }  // namespace csa2

@@ -301,9 +301,11 @@ __device__ __forceinline__ void locate_bin(uint32_t* shist, int* warp_tot, const
   *bstar = find_digit_t<NT>(shist, 2048, kk, warp_tot, above);
 }
 
-__global__ void __launch_bounds__(kTopkThreads)
+__global__ void __launch_bounds__(kTopkThreads, 2)   // two rows per SM (<= 32 registers)
 k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
        int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   const int64_t row = blockIdx.x;
@@ -373,6 +375,8 @@ k_topk_collect(const float* __restrict__ scores, int64_t stride, ValidSpec v, in
                const uint32_t* __restrict__ hist_in, int64_t hist_stride, uint32_t* __restrict__ sel_words,
                int64_t words_stride, uint32_t* __restrict__ cand_key, int32_t* __restrict__ cand_idx,
                int32_t* __restrict__ cand_count) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t shist[2048];
   __shared__ int warp_tot[kCollectThreads / 32];
   const int64_t row = blockIdx.y;
@@ -424,6 +428,8 @@ k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int
               int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride,
               const uint32_t* __restrict__ sel_words, int64_t words_stride, const uint32_t* __restrict__ cand_key,
               const int32_t* __restrict__ cand_idx, const int32_t* __restrict__ cand_count) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   const int64_t row = blockIdx.x;
@@ -463,6 +469,8 @@ k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int
 // 2048-bin key histograms of given score rows (for the split path on a given array).
 __global__ void __launch_bounds__(kCollectThreads)
 k_row_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, uint32_t* __restrict__ hist) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t sh[2048];
   const int64_t row = blockIdx.y;
   const int n = row_valid(v, row, stride);
@@ -496,8 +504,7 @@ cudaError_t launch_row_hist(const float* scores, int64_t rows, int64_t stride, V
   cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)rows * 2048 * 4, s);
   if (e != cudaSuccess) return e;
   dim3 g((unsigned)((stride + kCollectChunk - 1) / kCollectChunk), (unsigned)rows);
-  k_row_hist<<<g, kCollectThreads, 0, s>>>(scores, stride, v, hist);
-  return counted(cudaGetLastError());
+  return launch_step(k_row_hist, g, dim3(kCollectThreads), 0, s, scores, stride, v, hist);
 }
 
 size_t topk_split_scratch_bytes(int64_t rows, int64_t stride) {
@@ -518,23 +525,22 @@ cudaError_t launch_topk_split(const float* scores, int64_t rows, int64_t stride,
   cudaError_t e = cudaMemsetAsync(cand_count, 0, (size_t)rows * 16, s);
   if (e != cudaSuccess) return e;
   dim3 g1((unsigned)((stride + kCollectChunk - 1) / kCollectChunk), (unsigned)rows);
-  k_topk_collect<<<g1, kCollectThreads, 0, s>>>(scores, stride, v, k, hist, hist_stride, sel_words, words,
-                                                cand_key, cand_idx, cand_count);
-  e = counted(cudaGetLastError());
+  e = launch_step(k_topk_collect, g1, dim3(kCollectThreads), 0, s, scores, stride, v, k, hist, hist_stride,
+                  sel_words, words, cand_key, cand_idx, cand_count);
   if (e != cudaSuccess) return e;
   const size_t smem = sizeof(TopkSmem);
   e = cudaFuncSetAttribute(k_topk_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_topk_finish<<<(unsigned)rows, kTopkThreads, smem, s>>>(scores, stride, v, k, out_idx, out_cnt, remap, hist,
-                                                           hist_stride, sel_words, words, cand_key, cand_idx,
-                                                           cand_count);
-  return counted(cudaGetLastError());
+  return launch_step(k_topk_finish, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k, out_idx,
+                     out_cnt, remap, hist, hist_stride, sel_words, words, cand_key, cand_idx, cand_count);
 }
 
 // Block maxima: out[row][b] = max of scores[row][8b .. 8b+7] over the valid
 // columns, for b < ceil(n_valid / block).
 __global__ void k_block_max(const float* __restrict__ scores, int64_t stride, ValidSpec v, int block,
                             float* __restrict__ out, int64_t out_stride) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t row = blockIdx.y;
   const int n = row_valid(v, row, stride);
   const int nb = (n + block - 1) / block;
@@ -554,9 +560,8 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
   const size_t smem = sizeof(TopkSmem);
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  k_topk<<<(unsigned)rows, kTopkThreads, smem, s>>>(scores, stride, v, k, out_idx, out_cnt, remap, hist,
-                                                    hist_stride);
-  return counted(cudaGetLastError());
+  return launch_step(k_topk, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k, out_idx, out_cnt,
+                     remap, hist, hist_stride);
 }
 
 cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int block,
@@ -564,8 +569,7 @@ cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, 
   if (rows == 0) return cudaSuccess;
   const int64_t nb = (stride + block - 1) / block;
   dim3 grid((unsigned)((nb + 255) / 256), (unsigned)rows);
-  k_block_max<<<grid, 256, 0, s>>>(scores, stride, v, block, out, out_stride);
-  return counted(cudaGetLastError());
+  return launch_step(k_block_max, grid, dim3(256), 0, s, scores, stride, v, block, out, out_stride);
 }
 
 }  // namespace csa2
