@@ -301,7 +301,11 @@ __device__ __forceinline__ void locate_bin(uint32_t* shist, int* warp_tot, const
   *bstar = find_digit_t<NT>(shist, 2048, kk, warp_tot, above);
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 2)   // two rows per SM (<= 32 registers)
+// kB row elements per thread are loaded before any is used; kMinBlocks CTAs
+// (rows) per SM.  Few rows: <32, 1> (one round trip for a 32K-entry row);
+// many rows: <8, 2> (two rows per SM, <= 32 registers).
+template <int kB, int kMinBlocks>
+__global__ void __launch_bounds__(kTopkThreads, kMinBlocks)
 k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
        int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
   pdl_trigger();
@@ -335,26 +339,51 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
   const int words = (n + 31) / 32;
   for (int i = tid; i < words; i += kTopkThreads) sm.tie_bits[i] = 0;
   // one pass: higher bins -> selection bitmap; bin bstar -> candidate list
-  // (lanes of a warp cover one aligned 32-entry word, so the ballot is the word)
-  for (int j0 = 0; j0 < n; j0 += kTopkThreads * kBatch) {
-    float vv[kBatch];
+  // (lanes of a warp cover one aligned 32-entry word, so the ballot is the
+  // word); a batch's candidates are appended with one atomic per warp
+  for (int j0 = 0; j0 < n; j0 += kTopkThreads * kB) {
+    float vv[kB];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {   // independent loads first
+    for (int u = 0; u < kB; ++u) {   // independent loads first
       const int j = j0 + u * kTopkThreads + tid;
       vv[u] = j < n ? s[j] : 0.f;
     }
+    uint32_t cmask = 0;
+    int ccount = 0;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
+    for (int u = 0; u < kB; ++u) {
       const int j = j0 + u * kTopkThreads + tid;
-      uint32_t key = 0, bin = 0;
-      if (j < n) {
-        key = order_key(vv[u]);
-        bin = key >> 21;
-      }
+      uint32_t bin = 0;
+      if (j < n) bin = order_key(vv[u]) >> 21;
       const uint32_t word = __ballot_sync(0xffffffffu, j < n && bin > (uint32_t)bstar);
       if (lane == 0 && j < n) sm.sel_bits[j >> 5] = word;
-      const int pc = warp_slot(&sm.nC, j < n && bin == (uint32_t)bstar, kCandCap);
-      if (pc >= 0) { sm.ckey[pc] = key; sm.cidx[pc] = j; }
+      if (j < n && bin == (uint32_t)bstar) {
+        cmask |= 1u << u;
+        ++ccount;
+      }
+    }
+    int incl = ccount;   // warp prefix sum of the candidate counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+    if (wtot) {
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sm.nC, wtot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - ccount;
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        if ((cmask >> u) & 1u) {
+          if (pos < kCandCap) {
+            sm.ckey[pos] = order_key(vv[u]);
+            sm.cidx[pos] = j0 + u * kTopkThreads + tid;
+          }
+          ++pos;
+        }
+      }
     }
   }
   __syncthreads();
@@ -558,10 +587,20 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
                         int64_t hist_stride, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   const size_t smem = sizeof(TopkSmem);
-  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  return launch_step(k_topk, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k, out_idx, out_cnt,
-                     remap, hist, hist_stride);
+  if (rows <= sms) {   // one wave of rows: latency counts, occupancy does not
+    e = cudaFuncSetAttribute(k_topk<32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_step(k_topk<32, 1>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k,
+                       out_idx, out_cnt, remap, hist, hist_stride);
+  }
+  e = cudaFuncSetAttribute(k_topk<8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_step(k_topk<8, 2>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k, out_idx,
+                     out_cnt, remap, hist, hist_stride);
 }
 
 cudaError_t launch_block_max(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int block,

@@ -145,6 +145,24 @@ def test_topk_bit_exact(k, split):
         assert np.all(idx[r, cnt[r]:] == -1)
 
 
+@pytest.mark.parametrize("k", [512, 16])
+def test_topk_bit_exact_unaligned_rows(k):
+    """Rows that do not start on a 16-byte boundary (odd stride) take the
+    scalar-load pass; same selection rule."""
+    s, nv = _score_rows()
+    s = torch.nn.functional.pad(s, (0, 1), value=float("nan")).contiguous()   # stride 40,001
+    rows = s.shape[0]
+    idx = torch.full((rows, k), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
+    abi.csa2_topk_f32(s.cuda(), nv.cuda(), k, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for r in range(rows):
+        ref = I.topk(s[r, :nv[r]].numpy(), k)
+        assert cnt[r] == len(ref), r
+        assert np.array_equal(idx[r, :cnt[r]], ref), r
+        assert np.all(idx[r, cnt[r]:] == -1)
+
+
 def test_block_pool_bit_exact():
     s, nv = _score_rows()
     rows = s.shape[0]
