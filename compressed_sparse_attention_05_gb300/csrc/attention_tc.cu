@@ -13,8 +13,7 @@
 //   O^T [512 dims x 64 heads] += V_chunk^T [512 x 128] . P^T    (4 M-tiles x 8 MMAs, k = 16 keys)
 // K = V, so one dequantised shared-memory tile serves as the K-major A
 // operand of the first product and as the MN-major A operand of the second.
-// S^T is accumulated in four interleaved partial sums (4 x 64 tensor-memory
-// columns, summed by the softmax) and O^T in four M-tiles (4 x 64).  PV runs
+// S^T takes 64 tensor-memory columns and O^T four M-tiles of 64.  PV runs
 // tile by tile with a commit per tile, so that the next chunk's slice of the
 // K tile is rewritten as soon as the tile that read it is done.
 //
@@ -57,7 +56,7 @@ constexpr int kMaxChunks = 8;    // keys per token <= 1,024; also the largest po
 constexpr int kWorkers = 512;             // 16 warps: dequantisation and softmax
 constexpr int kThreads = kWorkers + 32;   // + one warp that allocates tensor memory and issues the MMAs
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;     // four partial S^T accumulators (k-step ks goes to ks % 4), 64 columns each
+constexpr uint32_t kColS = 0;     // S^T: 64 columns
 constexpr uint32_t kColO = 256;   // O^T: four M-tiles of 64 columns
 constexpr float kRescaleLog2 = 8.f;  // move a head's reference maximum only beyond this growth
 
@@ -282,25 +281,14 @@ __device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, in
   return -1;
 }
 
-// Scores of the thread's key for heads 16*hg .. +15, in the log2 domain:
-// the sum of the four partial S^T accumulators times scale*log2(e), or -inf
-// for a missing key.
+// Scores of the thread's key for heads 16*hg .. +15, in the log2 domain
+// (S^T times scale*log2(e)), or -inf for a missing key.
 __device__ __forceinline__ void load_scores(uint32_t tm, int hg, uint32_t lane_q, bool valid, float sl2,
                                             float (&x)[16]) {
-  float y[16];
   tc::tmem_ld16(tm + kColS + 16 * hg + lane_q, x);
-  tc::tmem_ld16(tm + kColS + 64 + 16 * hg + lane_q, y);
   tc::tmem_wait_ld();
 #pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] += y[j];
-  tc::tmem_ld16(tm + kColS + 128 + 16 * hg + lane_q, y);
-  tc::tmem_wait_ld();
-#pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] += y[j];
-  tc::tmem_ld16(tm + kColS + 192 + 16 * hg + lane_q, y);
-  tc::tmem_wait_ld();
-#pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = valid ? (x[j] + y[j]) * sl2 : -INFINITY;
+  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
 }
 
 // Bounded wait of a whole warp; on time-out the CTA's abort flag is raised.
@@ -443,8 +431,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
           tc::tc_fence_after();
 #pragma unroll
           for (int ks = 8 * sl; ks < 8 * sl + 8; ++ks)   // descriptor addresses advance in 16-byte units
-            tc::mma_f16(tm + kColS + 64 * (ks & 3), dk_s + (uint64_t)(ks * 16), dq_s + (uint64_t)(ks * 16), kIdS,
-                        ks >= 4);
+            tc::mma_f16(tm + kColS, dk_s + (uint64_t)(ks * 16), dq_s + (uint64_t)(ks * 16), kIdS, ks > 0);
         }
         if (!ok) { *abort = 1; break; }
         tc::mma_commit(&sm.bar_s);
