@@ -23,8 +23,9 @@
 // warp announces a written slice on an mbarrier and
 // the MMA warp issues the slice's eight S MMAs once all warps have, so
 // dequantisation overlaps the tensor core.  (An MMA issue blocks the issuing
-// thread while the tensor pipe is full, hence a warp of its own.)  A slice's registers are refilled
-// with the next chunk's bytes right after it is stored.  Softmax (thread = one key x 16 heads): the reference maximum of a
+// thread while the tensor pipe is full, hence a warp of its own.)  The next
+// chunk's bytes are requested together once the tile is written (loads spread
+// over the slices stall the slices that follow them).  Softmax (thread = one key x 16 heads): the reference maximum of a
 // head only moves when a score exceeds it by more than 2^8 (then O^T is
 // rescaled in tensor memory), so P = exp2(s - m) <= 256 fits fp16 and most
 // chunks need no maximum reduction at all; row sums stay per thread until
@@ -472,7 +473,6 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       const uint32_t pr = ((qd >> 1) ? w1 : w0) >> (16 * (qd & 1));                      \
       if (wok) store_slice<SL>(a, kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile);   \
     }                                                                                    \
-    if (it + 1 < n_my) load_slice<SL>(a, nxt_src, qd, kb);                               \
     tc::fence_async_smem();                                                              \
     __syncwarp();                                                                        \
     if (lane == 0) tc::mbar_arrive(&sm.k_ready[SL]);                                     \
@@ -482,6 +482,13 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       CSA2_SLICE(2)
       CSA2_SLICE(3)
 #undef CSA2_SLICE
+      // the next chunk's bytes, requested together once this chunk's tile is written
+      if (it + 1 < n_my) {
+        load_slice<0>(a, nxt_src, qd, kb);
+        load_slice<1>(a, nxt_src, qd, kb);
+        load_slice<2>(a, nxt_src, qd, kb);
+        load_slice<3>(a, nxt_src, qd, kb);
+      }
       const bool valid = sm.slot[it * kChunk + kc] != -1;   // the softmax thread's key
       cur_src = nxt_src;
       cur_wsc = load_wscale(a, nxt_src);
