@@ -80,15 +80,21 @@ __device__ __forceinline__ int block_exclusive_scan_t(int v, int* warp_tot) {
   __syncthreads();
   return before + x - v;
 }
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot) {
-  return block_exclusive_scan_t<kTopkThreads>(v, warp_tot);
+
+// Shared-memory reductions without a returned value (red.shared: the issuing
+// thread does not wait for them).
+__device__ __forceinline__ void red_add_shared(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_or_shared(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.or.b32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "r"(v) : "memory");
 }
 
 // Adds `digit` (< nbins, or >= nbins for "none") to a shared histogram: one
-// shared atomic per lane (match.any aggregation costs more than the rare
+// shared reduction per lane (match.any aggregation costs more than the rare
 // serialisation of equal digits).
 __device__ __forceinline__ void warp_hist_add(uint32_t* hist, uint32_t digit, uint32_t nbins) {
-  if (digit < nbins) atomicAdd(&hist[digit], 1u);
+  if (digit < nbins) red_add_shared(&hist[digit], 1u);
 }
 
 // Slot in a shared list for every lane with `take` (one atomic per warp); -1
@@ -132,9 +138,6 @@ __device__ __forceinline__ int find_digit_t(const uint32_t* hist, int bins, int 
   *above = s_above;
   return s_digit;
 }
-__device__ __forceinline__ int find_digit(const uint32_t* hist, int bins, int need, int* warp_tot, int* above) {
-  return find_digit_t<kTopkThreads>(hist, bins, need, warp_tot, above);
-}
 
 constexpr int kBitmapMax = 1 << 18;            // rows up to 262,144 entries use bitmaps
 constexpr int kBitmapWords = kBitmapMax / 32;
@@ -150,50 +153,78 @@ struct TopkSmem {
   uint32_t tie_bits[kBitmapWords];  // entries equal to the K-th key
 };
 
-// Selection from the candidates of the threshold bin: the sel bitmap already
-// holds every entry of a higher bin; find the exact K-th key among the
-// candidates, mark the candidates above it and the `need` lowest-index ties,
-// and write the selection in index order.
-__device__ void finish_from_candidates(TopkSmem& sm, int n, int kk, int bstar, int need, int nC,
-                                       int32_t* __restrict__ out, const Remap& remap, int64_t row) {
-  const int tid = threadIdx.x;
-  const int words = (n + 31) / 32;
+// The exact K-th key among keys[0 .. nC) by one warp: three 7-bit radix
+// passes below the 11-bit bin, with warp shuffles instead of block barriers
+// (few candidates).  *T_out = the K-th key, *need_out = entries equal to it
+// to take.
+template <class Sm>
+__device__ void warp_radix_threshold(Sm& sm, const uint32_t* keys, int nC, int bstar, int need, uint32_t* T_out,
+                                     int* need_out) {
+  const int lane = threadIdx.x & 31;
   uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
-  for (int p = 0; p < 3; ++p) {   // 3 radix passes of 7 bits over the candidates
+  for (int p = 0; p < 3; ++p) {
     const int sh = 14 - 7 * p;
-    const uint32_t nb = 128;
-    for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
-    __syncthreads();
-    for (int i0 = 0; i0 < nC; i0 += kTopkThreads) {
-      const int i = i0 + tid;
-      uint32_t dg = 0xFFFFFFFFu;
-      if (i < nC) {
-        const uint32_t key = sm.ckey[i];
-        if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
-      }
-      warp_hist_add(sm.hist2, dg, nb);
+    for (int i = lane; i < 128; i += 32) sm.hist2[i] = 0;
+    __syncwarp();
+    for (int i = lane; i < nC; i += 32) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) red_add_shared(&sm.hist2[(key >> sh) & 127u], 1u);
     }
-    __syncthreads();
-    int ab;
-    const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+    __syncwarp();
+    // lane L owns digits 127 - 4L .. 124 - 4L, highest first
+    uint32_t h[4];
+    int c = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      h[q] = sm.hist2[127 - 4 * lane - q];
+      c += (int)h[q];
+    }
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int before = incl - c;
+    const uint32_t hit = __ballot_sync(0xffffffffu, before < need && incl >= need);
+    const int L = hit ? __ffs(hit) - 1 : 0;   // the matching candidates always hold >= need entries
+    int dg = 0, ab = 0;
+    if (lane == L) {
+      int cum = before;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (cum + (int)h[q] >= need) {
+          dg = 127 - 4 * lane - q;
+          ab = cum;
+          break;
+        }
+        cum += (int)h[q];
+      }
+    }
+    dg = __shfl_sync(0xffffffffu, dg, L);
+    ab = __shfl_sync(0xffffffffu, ab, L);
     need -= ab;
     prefix |= (uint32_t)dg << sh;
-    mask |= (nb - 1) << sh;
+    mask |= 127u << sh;
+    __syncwarp();   // every lane has read hist2 before the next pass clears it
   }
-  const uint32_t T = prefix;             // exact K-th key; `need` entries equal to T are taken
-  for (int i = tid; i < nC; i += kTopkThreads) {
-    const uint32_t key = sm.ckey[i];
-    const int32_t j = sm.cidx[i];
-    if (key > T) atomicOr(&sm.sel_bits[j >> 5], 1u << (j & 31));
-    else if (key == T) atomicOr(&sm.tie_bits[j >> 5], 1u << (j & 31));
-  }
-  __syncthreads();
+  *T_out = prefix;
+  *need_out = need;
+}
+
+// Index-ordered output of the selection: sel_bits holds every selected entry
+// but the ties, tie_bits the entries equal to the K-th key, of which the
+// `need` lowest-index ones are taken.
+template <int NT, class Sm>
+__device__ void write_selection(Sm& sm, int words, int kk, int need, int32_t* __restrict__ out, const Remap& remap,
+                                int64_t row) {
+  const int tid = threadIdx.x;
   // index-ordered output: thread tid owns words [w0, w1)
-  const int per = (words + kTopkThreads - 1) / kTopkThreads;
+  const int per = (words + NT - 1) / NT;
   const int w0 = min(words, tid * per), w1 = min(words, w0 + per);
   int ties = 0;
   for (int w = w0; w < w1; ++w) ties += __popc(sm.tie_bits[w]);
-  int ties_before = block_exclusive_scan(ties, sm.warp_tot);
+  int ties_before = block_exclusive_scan_t<NT>(ties, sm.warp_tot);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) {
     uint32_t tb = sm.tie_bits[w];
@@ -205,7 +236,7 @@ __device__ void finish_from_candidates(TopkSmem& sm, int n, int kk, int bstar, i
     }
     cnt += __popc(sm.sel_bits[w]);
   }
-  int pos = block_exclusive_scan(cnt, sm.warp_tot);
+  int pos = block_exclusive_scan_t<NT>(cnt, sm.warp_tot);
   for (int w = w0; w < w1; ++w) {
     uint32_t sb = sm.sel_bits[w];
     while (sb) {
@@ -217,18 +248,77 @@ __device__ void finish_from_candidates(TopkSmem& sm, int n, int kk, int bstar, i
   }
 }
 
+// Selection from the candidates of the threshold bin: the sel bitmap already
+// holds every entry of a higher bin; find the exact K-th key among the
+// candidates, mark the candidates above it and the `need` lowest-index ties,
+// and write the selection in index order.
+template <int NT, class Sm, bool kWarpRadix = false>
+__device__ void finish_from_candidates(Sm& sm, int n, int kk, int bstar, int need, int nC,
+                                       int32_t* __restrict__ out, const Remap& remap, int64_t row) {
+  const int tid = threadIdx.x;
+  const int words = (n + 31) / 32;
+  uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
+  if (kWarpRadix) {
+    __shared__ uint32_t s_T;
+    __shared__ int s_need;
+    if (tid < 32) {
+      uint32_t t;
+      int nd;
+      warp_radix_threshold(sm, sm.ckey, nC, bstar, need, &t, &nd);
+      if (tid == 0) {
+        s_T = t;
+        s_need = nd;
+      }
+    }
+    __syncthreads();
+    prefix = s_T;
+    need = s_need;
+  }
+  for (int p = 0; p < (kWarpRadix ? 0 : 3); ++p) {   // 3 radix passes of 7 bits over the candidates
+    const int sh = 14 - 7 * p;
+    const uint32_t nb = 128;
+    for (int i = tid; i < (int)nb; i += NT) sm.hist2[i] = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < nC; i0 += NT) {
+      const int i = i0 + tid;
+      uint32_t dg = 0xFFFFFFFFu;
+      if (i < nC) {
+        const uint32_t key = sm.ckey[i];
+        if ((key & mask) == prefix) dg = (key >> sh) & (nb - 1);
+      }
+      warp_hist_add(sm.hist2, dg, nb);
+    }
+    __syncthreads();
+    int ab;
+    const int dg = find_digit_t<NT>(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+    need -= ab;
+    prefix |= (uint32_t)dg << sh;
+    mask |= (nb - 1) << sh;
+  }
+  const uint32_t T = prefix;             // exact K-th key; `need` entries equal to T are taken
+  for (int i = tid; i < nC; i += NT) {
+    const uint32_t key = sm.ckey[i];
+    const int32_t j = sm.cidx[i];
+    if (key > T) red_or_shared(&sm.sel_bits[j >> 5], 1u << (j & 31));
+    else if (key == T) red_or_shared(&sm.tie_bits[j >> 5], 1u << (j & 31));
+  }
+  __syncthreads();
+  write_selection<NT>(sm, words, kk, need, out, remap, row);
+}
+
 // Crowded threshold bin: radix select over the whole row from the 11-bit
 // prefix, then an index-ordered pass writes the selection.
-__device__ void radix_whole_row(TopkSmem& sm, const float* __restrict__ s, int n, int kk, int bstar, int need,
+template <int NT, class Sm>
+__device__ void radix_whole_row(Sm& sm, const float* __restrict__ s, int n, int kk, int bstar, int need,
                                 int32_t* __restrict__ out, const Remap& remap, int64_t row) {
   const int tid = threadIdx.x;
   uint32_t prefix = (uint32_t)bstar << 21, mask = 0xFFE00000u;
   for (int p = 0; p < 3; ++p) {
     const int sh = p == 0 ? 13 : (p == 1 ? 5 : 0);
     const uint32_t nb = p == 2 ? 32u : 256u;
-    for (int i = tid; i < (int)nb; i += kTopkThreads) sm.hist2[i] = 0;
+    for (int i = tid; i < (int)nb; i += NT) sm.hist2[i] = 0;
     __syncthreads();
-    for (int j0 = 0; j0 < n; j0 += kTopkThreads) {
+    for (int j0 = 0; j0 < n; j0 += NT) {
       const int j = j0 + tid;
       uint32_t dg = 0xFFFFFFFFu;
       if (j < n) {
@@ -239,13 +329,13 @@ __device__ void radix_whole_row(TopkSmem& sm, const float* __restrict__ s, int n
     }
     __syncthreads();
     int ab;
-    const int dg = find_digit(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
+    const int dg = find_digit_t<NT>(sm.hist2, (int)nb, need, sm.warp_tot, &ab);
     need -= ab;
     prefix |= (uint32_t)dg << sh;
     mask |= (nb - 1) << sh;
   }
   const uint32_t T = prefix;
-  const int chunk = (n + kTopkThreads - 1) / kTopkThreads;
+  const int chunk = (n + NT - 1) / NT;
   const int lo = min(n, tid * chunk), hi = min(n, lo + chunk);
   int gt = 0, eq = 0;
   for (int j = lo; j < hi; ++j) {
@@ -253,8 +343,8 @@ __device__ void radix_whole_row(TopkSmem& sm, const float* __restrict__ s, int n
     gt += key > T;
     eq += key == T;
   }
-  const int gt_before = block_exclusive_scan(gt, sm.warp_tot);
-  const int eq_before = block_exclusive_scan(eq, sm.warp_tot);
+  const int gt_before = block_exclusive_scan_t<NT>(gt, sm.warp_tot);
+  const int eq_before = block_exclusive_scan_t<NT>(eq, sm.warp_tot);
   int pos = gt_before + min(eq_before, need);
   int eq_seen = eq_before;
   for (int j = lo; j < hi; ++j) {
@@ -333,7 +423,7 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
   const int need = kk - above;           // entries of bin bstar to take
   const int n_bin = (int)sm.hist[bstar];
   if (n_bin > kCandCap || n > kBitmapMax) {
-    radix_whole_row(sm, s, n, kk, bstar, need, out, remap, row);
+    radix_whole_row<kTopkThreads>(sm, s, n, kk, bstar, need, out, remap, row);
     return;
   }
   const int words = (n + 31) / 32;
@@ -387,7 +477,235 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
     }
   }
   __syncthreads();
-  finish_from_candidates(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
+  finish_from_candidates<kTopkThreads>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
+}
+
+// ---- many short rows (prefill: one row per query token) ------------------------------
+// Rows of at most 32,768 entries, many more rows than SMs: a 256-thread CTA
+// per row, four rows per SM, and few instructions per entry.  A sample of the
+// row (64 spread runs of 16 entries) gives a lower bound for the K-th key: the
+// bin of the sample's r-th largest key, r about twice the sample's expected
+// share of the Top-K.  One pass over the row then compares every entry with
+// that bound as a float and keeps only the entries at or above it (their
+// keys, indices and 2048-bin histogram) in shared memory; the exact
+// selection (threshold bin, radix passes, ties by lower index, index-ordered
+// output) runs over those candidates.  When the bound was too high (fewer
+// than K candidates) or too low (more than fit), the row is selected by radix
+// passes over the whole row instead.
+constexpr int kShortThreads = 256;
+constexpr int kShortMaxN = 32768;
+constexpr int kShortCap = 4096;     // candidates kept in shared memory
+constexpr int kShortBatch = 16;     // row elements per thread loaded before any is used
+constexpr int kSample = 1024;       // 64 runs of 16 entries
+
+struct TopkShortSmem {
+  uint32_t hist[2048];
+  uint32_t hist2[256];
+  int warp_tot[kShortThreads / 32];
+  int nC, nB;
+  uint32_t ckey[kShortCap];
+  int32_t cidx[kShortCap];
+  uint32_t sel_bits[kShortMaxN / 32];
+  uint32_t tie_bits[kShortMaxN / 32];
+};
+
+// Element u of the thread's batch: with kVec, four consecutive entries per float4.
+template <bool kVec>
+__device__ __forceinline__ int batch_index(int j0, int tid, int u) {
+  return kVec ? j0 + 4 * ((u >> 2) * kShortThreads + tid) + (u & 3) : j0 + u * kShortThreads + tid;
+}
+template <bool kVec>
+__device__ __forceinline__ void load_batch(const float* __restrict__ s, int n, int j0, int tid,
+                                           float (&x)[kShortBatch]) {
+  if (kVec) {
+#pragma unroll
+    for (int u = 0; u < kShortBatch / 4; ++u) {
+      const int j = batch_index<true>(j0, tid, 4 * u);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j + 3 < n) {
+        f = *reinterpret_cast<const float4*>(s + j);
+      } else if (j < n) {
+        f.x = s[j];
+        if (j + 1 < n) f.y = s[j + 1];
+        if (j + 2 < n) f.z = s[j + 2];
+      }
+      x[4 * u] = f.x; x[4 * u + 1] = f.y; x[4 * u + 2] = f.z; x[4 * u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kShortBatch; ++u) {
+      const int j = batch_index<false>(j0, tid, u);
+      x[u] = j < n ? s[j] : 0.f;
+    }
+  }
+}
+// The float whose order_key is `key` (key > 0).
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kShortThreads, 4)
+k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+             int32_t* __restrict__ out_cnt, Remap remap) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkShortSmem& sm = *reinterpret_cast<TopkShortSmem*>(smem_raw);
+  constexpr int NT = kShortThreads;
+  constexpr int kStep = kShortBatch * NT;   // entries per batch
+  const int64_t row = blockIdx.x;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);   // <= stride <= kShortMaxN (checked by the launcher)
+  const int kk = min(k, n);
+  int32_t* out = out_idx + row * (int64_t)k;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  for (int j = kk + tid; j < k; j += NT) out[j] = -1;
+  if (tid == 0) out_cnt[row] = kk;
+  if (kk == 0) return;
+  if (kk == n) {
+    for (int j = tid; j < n; j += NT) out[j] = remap_index(remap, row, j);
+    return;
+  }
+  const int words = (n + 31) / 32;
+  for (int i = tid; i < words; i += NT) {
+    sm.sel_bits[i] = 0;
+    sm.tie_bits[i] = 0;
+  }
+  for (int i = tid; i < 2048; i += NT) sm.hist[i] = 0;
+  if (tid == 0) sm.nC = 0;
+  __syncthreads();
+
+  // ---- lower bound of the K-th key from the sample (rows longer than 2 x the sample)
+  bool take_all = true;
+  float f_lo = 0.f;
+  if (n > 2 * kSample) {
+    const int run = tid >> 2;   // 64 runs of 16 entries, thread = 4 of them
+    const int j = ((int)(((int64_t)run * (n - 16)) / 63) & ~3) + 4 * (tid & 3);
+    float x[4];
+    if (kVec) {
+      const float4 f = *reinterpret_cast<const float4*>(s + j);
+      x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = s[j + u];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) warp_hist_add(sm.hist, order_key(x[u]) >> 21, 2048);
+    __syncthreads();
+    const int r = min(kSample, (int)((2LL * kk * kSample + n - 1) / n) + 8);
+    int ab;
+    const int b_lo = find_digit_t<NT>(sm.hist, 2048, r, sm.warp_tot, &ab);
+    if (b_lo > 0) {
+      take_all = false;
+      f_lo = key_float((uint32_t)b_lo << 21);
+    }
+    for (int i = tid; i < 2048; i += NT) sm.hist[i] = 0;
+    __syncthreads();
+  }
+
+  // ---- one pass: entries at or above the bound -> candidates and their histogram
+  for (int j0 = 0; j0 < n; j0 += kStep) {
+    float x[kShortBatch];
+    load_batch<kVec>(s, n, j0, tid, x);
+    uint32_t cm = 0;
+#pragma unroll
+    for (int u = 0; u < kShortBatch; ++u)
+      if (batch_index<kVec>(j0, tid, u) < n && (take_all || x[u] >= f_lo)) cm |= 1u << u;
+    const int c = __popc(cm);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+    if (wtot) {
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sm.nC, wtot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - c;
+#pragma unroll
+      for (int u = 0; u < kShortBatch; ++u) {
+        if ((cm >> u) & 1u) {
+          const uint32_t key = order_key(x[u]);
+          if (pos < kShortCap) {
+            sm.ckey[pos] = key;
+            sm.cidx[pos] = batch_index<kVec>(j0, tid, u);
+          }
+          warp_hist_add(sm.hist, key >> 21, 2048);
+          ++pos;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int nC = sm.nC;
+  int above;
+  if (nC >= kk && nC <= kShortCap) {   // the candidates hold the Top-K
+    const int bstar = find_digit_t<NT>(sm.hist, 2048, kk, sm.warp_tot, &above);
+    // higher bins -> selected; the threshold bin's candidates -> a short list
+    // (keys in hist[0 .. 1024), indices in hist[1024 ..): the histogram is done)
+    if (tid == 0) sm.nB = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < nC; i0 += NT) {
+      const int i = i0 + tid;
+      uint32_t key = 0;
+      int32_t j = 0;
+      if (i < nC) {
+        key = sm.ckey[i];
+        j = sm.cidx[i];
+        if ((key >> 21) > (uint32_t)bstar) red_or_shared(&sm.sel_bits[j >> 5], 1u << (j & 31));
+      }
+      const int slot = warp_slot(&sm.nB, i < nC && (key >> 21) == (uint32_t)bstar, 1024);
+      if (slot >= 0) {
+        sm.hist[slot] = key;
+        sm.hist[1024 + slot] = (uint32_t)j;
+      }
+    }
+    __syncthreads();
+    const int nB = sm.nB;
+    if (nB > 1024) {   // crowded threshold bin: block-wide radix passes over all candidates
+      finish_from_candidates<NT>(sm, n, kk, bstar, kk - above, nC, out, remap, row);
+      return;
+    }
+    __shared__ uint32_t s_T;
+    __shared__ int s_need;
+    if (tid < 32) {
+      uint32_t t;
+      int nd;
+      warp_radix_threshold(sm, sm.hist, nB, bstar, kk - above, &t, &nd);
+      if (tid == 0) {
+        s_T = t;
+        s_need = nd;
+      }
+    }
+    __syncthreads();
+    const uint32_t T = s_T;
+    for (int i = tid; i < nB; i += NT) {
+      const uint32_t key = sm.hist[i];
+      const int32_t j = (int32_t)sm.hist[1024 + i];
+      if (key > T) red_or_shared(&sm.sel_bits[j >> 5], 1u << (j & 31));
+      else if (key == T) red_or_shared(&sm.tie_bits[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    write_selection<NT>(sm, words, kk, s_need, out, remap, row);
+    return;
+  }
+  // the bound missed: the whole row's histogram, then radix passes over the row
+  for (int i = tid; i < 2048; i += NT) sm.hist[i] = 0;
+  __syncthreads();
+  for (int j0 = 0; j0 < n; j0 += kStep) {
+    float x[kShortBatch];
+    load_batch<kVec>(s, n, j0, tid, x);
+#pragma unroll
+    for (int u = 0; u < kShortBatch; ++u)
+      warp_hist_add(sm.hist, batch_index<kVec>(j0, tid, u) < n ? order_key(x[u]) >> 21 : 0xFFFFFFFFu, 2048);
+  }
+  __syncthreads();
+  const int bstar = find_digit_t<NT>(sm.hist, 2048, kk, sm.warp_tot, &above);
+  radix_whole_row<NT>(sm, s, n, kk, bstar, kk - above, out, remap, row);
 }
 
 // ---- split Top-K: few, long rows ---------------------------------------------------
@@ -478,7 +796,7 @@ k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int
   locate_bin<kTopkThreads>(sm.hist, sm.warp_tot, s, n, kk, hist_in + row * hist_stride, &bstar, &above);
   const int need = kk - above;
   if ((int)sm.hist[bstar] > kCandCap || n > kBitmapMax) {
-    radix_whole_row(sm, s, n, kk, bstar, need, out, remap, row);
+    radix_whole_row<kTopkThreads>(sm, s, n, kk, bstar, need, out, remap, row);
     return;
   }
   const int words = (n + 31) / 32;
@@ -492,7 +810,7 @@ k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int
     sm.cidx[i] = cand_idx[row * kCandCap + i];
   }
   __syncthreads();
-  finish_from_candidates(sm, n, kk, bstar, need, nC, out, remap, row);
+  finish_from_candidates<kTopkThreads>(sm, n, kk, bstar, need, nC, out, remap, row);
 }
 
 // 2048-bin key histograms of given score rows (for the split path on a given array).
@@ -591,6 +909,20 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  if (rows >= 2 * (int64_t)sms && stride <= kShortMaxN) {   // many short rows
+    const size_t ssm = sizeof(TopkShortSmem);
+    const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
+    if (vec) {
+      e = cudaFuncSetAttribute(k_topk_short<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+      if (e != cudaSuccess) return e;
+      return launch_step(k_topk_short<true>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
+                         out_idx, out_cnt, remap);
+    }
+    e = cudaFuncSetAttribute(k_topk_short<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+    if (e != cudaSuccess) return e;
+    return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
+                       out_idx, out_cnt, remap);
+  }
   if (rows <= sms) {   // one wave of rows: latency counts, occupancy does not
     e = cudaFuncSetAttribute(k_topk<32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -163,6 +163,55 @@ def test_topk_bit_exact_unaligned_rows(k):
         assert np.all(idx[r, cnt[r]:] == -1)
 
 
+def _many_short_rows(stride):
+    """320 rows (more than twice the SM count) of at most 32,768 entries: the
+    four-rows-per-SM path (sampled lower bound, candidates only; the whole-row
+    radix fallback for rows of equal or crowded scores), vectorised when rows
+    are 16-byte aligned."""
+    g = torch.Generator().manual_seed(16)
+    kinds = ["normal", "ties", "ties2", "zeros", "neg", "const", "narrow", "normal"]
+    rows, n_valid = [], []
+    for r in range(320):
+        kind = kinds[r % len(kinds)]
+        n = [stride, stride - 3, 513, 512, 300, 0, 1, 4097, stride // 2 + 1][r % 9]
+        if kind == "normal":
+            x = torch.randn(stride, generator=g)
+        elif kind == "ties":
+            x = torch.randint(-20, 20, (stride,), generator=g).float() * 0.5
+        elif kind == "ties2":
+            x = torch.randint(0, 3, (stride,), generator=g).float()
+        elif kind == "zeros":
+            x = torch.zeros(stride)
+            x[torch.randperm(stride, generator=g)[:200]] = -0.0
+            x[5] = 1.0
+        elif kind == "const":
+            x = torch.full((stride,), 2.5)
+        elif kind == "narrow":
+            x = 1.0 + torch.rand(stride, generator=g) * 0.2
+        else:
+            x = -torch.rand(stride, generator=g) * 1e-30 - 1e-38
+        x[n:] = float("nan")   # never read: beyond the valid count
+        rows.append(x)
+        n_valid.append(n)
+    return torch.stack(rows).contiguous(), torch.tensor(n_valid, dtype=torch.int32)
+
+
+@pytest.mark.parametrize("stride", [16384, 12001, 32768])
+@pytest.mark.parametrize("k", [512, 7])
+def test_topk_bit_exact_many_short_rows(stride, k):
+    s, nv = _many_short_rows(stride)
+    rows = s.shape[0]
+    idx = torch.full((rows, k), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
+    abi.csa2_topk_f32(s.cuda(), nv.cuda(), k, idx, cnt)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for r in range(rows):
+        ref = I.topk(s[r, :nv[r]].numpy(), k)
+        assert cnt[r] == len(ref), r
+        assert np.array_equal(idx[r, :cnt[r]], ref), r
+        assert np.all(idx[r, cnt[r]:] == -1)
+
+
 def test_block_pool_bit_exact():
     s, nv = _score_rows()
     rows = s.shape[0]
