@@ -484,8 +484,8 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
 // Rows of at most 32,768 entries, many more rows than SMs: a 256-thread CTA
 // per row, four rows per SM, and few instructions per entry.  A sample of the
 // row (64 spread runs of 16 entries) gives a lower bound for the K-th key: the
-// bin of the sample's r-th largest key, r about twice the sample's expected
-// share of the Top-K.  One pass over the row then compares every entry with
+// bin of the sample's r-th largest key, r = 1.5 times the sample's expected
+// share of the Top-K plus 8.  One pass over the row then compares every entry with
 // that bound as a float and keeps only the entries at or above it (their
 // keys, indices and 2048-bin histogram) in shared memory; the exact
 // selection (threshold bin, radix passes, ties by lower index, index-ordered
@@ -544,6 +544,44 @@ __device__ __forceinline__ float key_float(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// Appends the batch's entries at or above f_lo (all of them with take_all) to
+// the candidates (one atomic per warp) and adds their keys to the histogram.
+template <bool kVec>
+__device__ __forceinline__ void collect_batch(TopkShortSmem& sm, const float (&x)[kShortBatch], int j0, int n,
+                                              bool take_all, float f_lo, int tid) {
+  const int lane = tid & 31;
+  uint32_t cm = 0;
+#pragma unroll
+  for (int u = 0; u < kShortBatch; ++u)
+    if (batch_index<kVec>(j0, tid, u) < n && (take_all || x[u] >= f_lo)) cm |= 1u << u;
+  const int c = __popc(cm);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+  if (wtot) {
+    int base = 0;
+    if (lane == 31) base = atomicAdd(&sm.nC, wtot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + incl - c;
+#pragma unroll
+    for (int u = 0; u < kShortBatch; ++u) {
+      if ((cm >> u) & 1u) {
+        const uint32_t key = order_key(x[u]);
+        if (pos < kShortCap) {
+          sm.ckey[pos] = key;
+          sm.cidx[pos] = batch_index<kVec>(j0, tid, u);
+        }
+        warp_hist_add(sm.hist, key >> 21, 2048);
+        ++pos;
+      }
+    }
+  }
+}
+
 template <bool kVec>
 __global__ void __launch_bounds__(kShortThreads, 4)
 k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
@@ -577,6 +615,9 @@ k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int 
   if (tid == 0) sm.nC = 0;
   __syncthreads();
 
+  // the first batch of the row is requested before the sample is analysed
+  float x0[kShortBatch];
+  load_batch<kVec>(s, n, 0, tid, x0);
   // ---- lower bound of the K-th key from the sample (rows longer than 2 x the sample)
   bool take_all = true;
   float f_lo = 0.f;
@@ -594,7 +635,7 @@ k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int 
 #pragma unroll
     for (int u = 0; u < 4; ++u) warp_hist_add(sm.hist, order_key(x[u]) >> 21, 2048);
     __syncthreads();
-    const int r = min(kSample, (int)((2LL * kk * kSample + n - 1) / n) + 8);
+    const int r = min(kSample, (int)((3LL * kk * kSample + 2 * n - 1) / (2 * n)) + 8);   // 1.5 x the expected share
     int ab;
     const int b_lo = find_digit_t<NT>(sm.hist, 2048, r, sm.warp_tot, &ab);
     if (b_lo > 0) {
@@ -606,39 +647,11 @@ k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int 
   }
 
   // ---- one pass: entries at or above the bound -> candidates and their histogram
-  for (int j0 = 0; j0 < n; j0 += kStep) {
+  collect_batch<kVec>(sm, x0, 0, n, take_all, f_lo, tid);
+  for (int j0 = kStep; j0 < n; j0 += kStep) {
     float x[kShortBatch];
     load_batch<kVec>(s, n, j0, tid, x);
-    uint32_t cm = 0;
-#pragma unroll
-    for (int u = 0; u < kShortBatch; ++u)
-      if (batch_index<kVec>(j0, tid, u) < n && (take_all || x[u] >= f_lo)) cm |= 1u << u;
-    const int c = __popc(cm);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-    if (wtot) {
-      int base = 0;
-      if (lane == 31) base = atomicAdd(&sm.nC, wtot);
-      base = __shfl_sync(0xffffffffu, base, 31);
-      int pos = base + incl - c;
-#pragma unroll
-      for (int u = 0; u < kShortBatch; ++u) {
-        if ((cm >> u) & 1u) {
-          const uint32_t key = order_key(x[u]);
-          if (pos < kShortCap) {
-            sm.ckey[pos] = key;
-            sm.cidx[pos] = batch_index<kVec>(j0, tid, u);
-          }
-          warp_hist_add(sm.hist, key >> 21, 2048);
-          ++pos;
-        }
-      }
-    }
+    collect_batch<kVec>(sm, x, j0, n, take_all, f_lo, tid);
   }
   __syncthreads();
   const int nC = sm.nC;
