@@ -7,11 +7,16 @@
 // [W; W_idx] (d + Di output channels) in one pass over A and writes split-K
 // fp32 partials; the epilogue kernel (pack.cu) sums the splits in a fixed
 // order, applies RMSNorm + RoPE + MXFP4 and stores the paged entry and its
-// indexer key.  Tensor cores: m16n8k16 bf16, fp32 accumulate, 128x128x32
-// CTA tiles, cp.async double buffering.
+// indexer key.  The main kernel runs on the fifth-generation tensor cores
+// (tcgen05, TMA-fed); an mma.sync kernel (m16n8k16 bf16, fp32 accumulate,
+// 128x128x32 CTA tiles, cp.async double buffering) takes the shapes it does
+// not (d not a multiple of 128, H not a multiple of 16).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
+#include "tma.cuh"
 
 namespace csa2 {
 
@@ -46,14 +51,16 @@ __device__ __forceinline__ void g_mma(float (&d)[4], uint32_t a0, uint32_t a1, u
 // grid = (N tiles, M tiles, splits).  8 warps as 2 (M) x 4 (N), warp tile 64 x 32.
 __global__ void __launch_bounds__(kGThreads)
 k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const uint16_t* __restrict__ W,
-                int d, const uint16_t* __restrict__ W_idx, int Di, int M, int k_per_split,
-                float* __restrict__ partials) {
+                int d, const uint16_t* __restrict__ W_idx, int Di, int M, float* __restrict__ partials) {
   __shared__ __align__(16) uint16_t sa[2][kGM * kGS];
   __shared__ __align__(16) uint16_t sb[2][kGN * kGS];
   const int N = d + Di;
   const int64_t Kd = 4LL * H;
   const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
-  const int kbeg = blockIdx.z * k_per_split;
+  // split blockIdx.z of gridDim.z takes K steps [st0, st1)
+  const int steps = (int)(Kd / kGK);
+  const int st0 = (int)((int64_t)blockIdx.z * steps / gridDim.z), st1 = (int)((int64_t)(blockIdx.z + 1) * steps / gridDim.z);
+  const int kbeg = st0 * kGK;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wm = warp >> 2, wn = warp & 3;
 
@@ -91,8 +98,8 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j][0] = acc[i][j][1] = acc[i][j][2] = acc[i][j][3] = 0.f;
 
-  const int n_iter = k_per_split / kGK;
-  load_stage(0, kbeg);
+  const int n_iter = st1 - st0;
+  if (n_iter > 0) load_stage(0, kbeg);
   for (int it = 0; it < n_iter; ++it) {
     const int st = it & 1;
     cp_async_wait_all();
@@ -138,147 +145,149 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
     }
 }
 
-// ---- tcgen05 path ----------------------------------------------------------------
-// CTA tile 128 (M) x 128 (N) x 64 (K) per stage, 4-stage ring of operands in the
-// 128-byte-swizzled K-major layout (8-row atoms of 1024 B, 16-byte chunk index
-// XOR row % 8) written by cp.async; thread 0 issues tcgen05.mma (M=128, N=128,
-// K=16) into a 128-column fp32 TMEM accumulator and commits each stage to an
-// mbarrier that frees its buffers.  Every wait is bounded.
-constexpr int kTcM = 128, kTcN = 128, kTcK = 64, kTcStages = 4, kTcThreads = 128;
-constexpr int kTcStageBytes = (kTcM + kTcN) * kTcK * 2;   // 32 KB
+// ---- tcgen05 + TMA path -------------------------------------------------------------
+// CTA tile 128 entries x 128 output channels; K in 64-wide stages of 32 KB
+// (A then B, both 128-byte-swizzled K-major) in a 6-stage ring filled by
+// tensor-map copies: A is the hidden states seen as [B][G][4H] (row j of
+// batch b starts at token 4j), B is W or W_idx.  Warp 0 issues the copies,
+// warp 1 the MMAs (M = 128, N = 128, K = 16) into a 128-column fp32
+// accumulator in tensor memory, warps 2..5 write the fp32 partial sums.
+// Split K: grid.z = B x n_split, split s takes stages [s n / n_split,
+// (s + 1) n / n_split).  Every wait is bounded.
+constexpr int kTmM = 128, kTmN = 128, kTmK = 64, kTmStages = 6;
+constexpr int kTmABytes = kTmM * kTmK * 2;                 // 16 KB
+constexpr int kTmStageBytes = kTmABytes + kTmN * kTmK * 2;   // 32 KB
+constexpr int kTmEpiWarps = 4;
+constexpr int kTmThreads = (2 + kTmEpiWarps) * 32;
+constexpr int kTmSmsTarget = 152;   // splits fill this many SMs once (the GPU's SM count)
 
-__global__ void __launch_bounds__(kTcThreads)
-k_compress_gemm_tc(const uint16_t* __restrict__ hidden, int G, int T, int H, const uint16_t* __restrict__ W,
-                   int d, const uint16_t* __restrict__ W_idx, int Di, int M, int k_per_split,
-                   float* __restrict__ partials, uint32_t* status) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  __shared__ uint64_t bar_free[kTcStages];
-  __shared__ uint64_t bar_done;
-  __shared__ uint32_t tmem_slot;
+struct CompressSmem {
+  unsigned char ring[kTmStages][kTmStageBytes];
+  uint64_t full[kTmStages], empty[kTmStages], acc_full;
+  uint32_t tmem;
+  int abort;
+};
+
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255) == 255 && *abort) return false;
+  }
+  *abort = 1;
+  return false;
+}
+
+__global__ void __launch_bounds__(kTmThreads, 1)
+k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
+                    const __grid_constant__ CUtensorMap imap, int G, int d, int N, int M, int n_stages, int n_split,
+                    float* __restrict__ partials, uint32_t* status) {
+  extern __shared__ unsigned char smem_raw[];
   pdl_trigger();
   pdl_wait();
   const uint32_t pad = (1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u;
-  unsigned char* ring = smem_raw + pad;
-  const int N = d + Di;
-  const int64_t Kd = 4LL * H;
-  const int m0 = blockIdx.y * kTcM, n0 = blockIdx.x * kTcN;
-  const int kbeg = blockIdx.z * k_per_split;
-  const int n_iter = k_per_split / kTcK;
+  CompressSmem& sm = *reinterpret_cast<CompressSmem*>(smem_raw + pad);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kTmN, j0 = blockIdx.y * kTmM;
+  const int b = blockIdx.z / n_split, split = blockIdx.z % n_split;
+  const int s0 = (int)((int64_t)split * n_stages / n_split);
+  const int my = (int)((int64_t)(split + 1) * n_stages / n_split) - s0;
 
   if (tid == 0) {
-    for (int i = 0; i < kTcStages; ++i) tc::mbar_init(&bar_free[i], 1);
-    tc::mbar_init(&bar_done, 1);
+    for (int i = 0; i < kTmStages; ++i) {
+      tc::mbar_init(&sm.full[i], 1);
+      tc::mbar_init(&sm.empty[i], 1);
+    }
+    tc::mbar_init(&sm.acc_full, 1);
+    sm.abort = 0;
     tc::mbar_fence_init();
   }
-  if (warp == 0) tc::tmem_alloc(&tmem_slot, kTcN);
+  if (warp == 1) tc::tmem_alloc(&sm.tmem, kTmN);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  const uint32_t tmem = tmem_slot;
+  const uint32_t tm = sm.tmem;
+  volatile int* abort = &sm.abort;
 
-  // row sources: this thread copies rows (tid / 8) + 16 i, 16-byte chunk tid % 8
-  const int c16 = tid & 7;
-  auto stage_ptr = [&](int st) { return ring + st * kTcStageBytes; };
-  auto issue_loads = [&](int st, int k0) {
-    unsigned char* sa = stage_ptr(st);
-    unsigned char* sb = sa + kTcM * kTcK * 2;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = (tid >> 3) + 16 * i;
-      const uint32_t off = (r >> 3) * 1024 + (r & 7) * 128 + ((c16 ^ (r & 7)) << 4);
-      const int m = m0 + r;
-      const bool okA = m < M;
-      const int mm = okA ? m : 0;
-      const uint16_t* ga = hidden + ((int64_t)(mm / G) * T + 4LL * (mm % G)) * H + k0 + c16 * 8;
-      const int n = n0 + r;
-      const bool okB = n < N;
-      const uint16_t* gb = !okB ? W : (n < d ? W + (int64_t)n * Kd : W_idx + (int64_t)(n - d) * Kd);
-      gb += okB ? k0 + c16 * 8 : 0;
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_addr(sa + off)), "l"(ga),
-                   "r"(okA ? 16 : 0));
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(tc::smem_addr(sb + off)), "l"(gb),
-                   "r"(okB ? 16 : 0));
-    }
-    asm volatile("cp.async.commit_group;\n");
-  };
-
-  constexpr uint32_t idesc = tc::idesc_f16(kTcM, kTcN, 1, 0, 0);
-  bool ok = true;
-  // prologue: stages 0 .. S-2
-  for (int i = 0; i < kTcStages - 1; ++i) {
-    if (i < n_iter) issue_loads(i, kbeg + i * kTcK);
-    else asm volatile("cp.async.commit_group;\n");
-  }
-  for (int it = 0; it < n_iter; ++it) {
-    // refill the stage that chunk it + S - 1 goes to, once its previous MMA is done;
-    // the block votes so that every thread takes the same branch after a timeout
-    const int nxt = it + kTcStages - 1;
-    bool okw = true;
-    if (nxt < n_iter && nxt >= kTcStages) okw = tc::mbar_wait(&bar_free[nxt % kTcStages], ((nxt / kTcStages) - 1) & 1);
-    ok = __syncthreads_and(okw) != 0;
-    if (!ok) break;
-    if (nxt < n_iter) issue_loads(nxt % kTcStages, kbeg + nxt * kTcK);
-    else asm volatile("cp.async.commit_group;\n");
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(kTcStages - 1));
-    tc::fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc::tc_fence_after();
-      const int st = it % kTcStages;
-      const uint32_t sa = tc::smem_addr(stage_ptr(st));
-      const uint32_t sb = sa + kTcM * kTcK * 2;
-#pragma unroll
-      for (int ks = 0; ks < kTcK / 16; ++ks) {
-        const uint64_t ad = tc::smem_desc(sa + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
-        const uint64_t bd = tc::smem_desc(sb + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
-        tc::mma_f16(tmem, ad, bd, idesc, (it > 0 || ks > 0) ? 1u : 0u);
+  if (warp == 0) {
+    // ================= producer =================
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < my; ++i) {
+        const int st = i % kTmStages;
+        if (i >= kTmStages && !wait_or_abort(&sm.empty[st], ((i / kTmStages) - 1) & 1, abort)) break;
+        tc::mbar_arrive_expect_tx(&sm.full[st], kTmStageBytes);
+        const int kx = (s0 + i) * kTmK;
+        tma::load_3d(sm.ring[st], &amap, kx, j0, b, &sm.full[st]);
+        if (n0 < d) tma::load_2d(sm.ring[st] + kTmABytes, &wmap, kx, n0, &sm.full[st]);
+        else tma::load_2d(sm.ring[st] + kTmABytes, &imap, kx, n0 - d, &sm.full[st]);
+        issued = i + 1;
       }
-      tc::mma_commit(&bar_free[st]);
-      if (it == n_iter - 1) tc::mma_commit(&bar_done);
+      for (int i = max(0, issued - kTmStages); i < issued; ++i)   // every issued copy lands before exit
+        for (uint32_t k = 0; k < (1u << 22); ++k)
+          if (tc::mbar_try_wait(&sm.full[i % kTmStages], (i / kTmStages) & 1)) break;
     }
-  }
-  asm volatile("cp.async.wait_group 0;\n");
-  if (ok && n_iter > 0) ok = __syncthreads_and(tc::mbar_wait(&bar_done, 0)) != 0;
-  if (!ok && tid == 0) raise_status(status, CSA2_STATUS_TIMEOUT);
-  tc::tc_fence_after();
-  if (ok && n_iter > 0) {
-    // epilogue: lane (32 warp + lane) holds row m0 + 32 warp + lane
-    const int m = m0 + warp * 32 + lane;
-    float* out = partials + (int64_t)blockIdx.z * M * N + (int64_t)m * N + n0;
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issue =================
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_f16(kTmM, kTmN, 1, 0, 0);   // bf16, K-major A and B
+      for (int i = 0; i < my; ++i) {
+        const int st = i % kTmStages;
+        if (!wait_or_abort(&sm.full[st], (i / kTmStages) & 1, abort)) break;
+        tc::tc_fence_after();
+        const uint32_t sa = tc::smem_addr(sm.ring[st]), sb = sa + kTmABytes;
+#pragma unroll
+        for (int ks = 0; ks < kTmK / 16; ++ks) {
+          const uint64_t ad = tc::smem_desc(sa + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
+          const uint64_t bd = tc::smem_desc(sb + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
+          tc::mma_f16(tm, ad, bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&sm.empty[st]);
+      }
+      tc::mma_commit(&sm.acc_full);   // arrives once every MMA issued above is complete
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue: warp w reads lane quarter w % 4 =================
+    const int q = warp & 3;
+    const bool ok = __all_sync(0xffffffffu, wait_or_abort(&sm.acc_full, 0, abort));
+    tc::tc_fence_after();
+    if (ok && !*abort && my > 0) {
+      const int j = j0 + 32 * q + lane;
+      float* out = partials + ((int64_t)split * M + (int64_t)b * G + j) * N + n0;
 #pragma unroll 1
-    for (int c = 0; c < kTcN; c += 16) {
-      float v[16];
-      tc::tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + c, v);
-      tc::tmem_wait_ld();
-      if (m < M) {
+      for (int c = 0; c < kTmN; c += 16) {
+        float v[16];
+        tc::tmem_ld16(tm + ((uint32_t)(32 * q) << 16) + c, v);
+        tc::tmem_wait_ld();
+        if (j < G) {
 #pragma unroll
-        for (int q = 0; q < 16; q += 4)
-          if (n0 + c + q < N) *reinterpret_cast<float4*>(out + c + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+          for (int u = 0; u < 16; u += 4)
+            if (n0 + c + u < N) *reinterpret_cast<float4*>(out + c + u) = make_float4(v[u], v[u + 1], v[u + 2], v[u + 3]);
+        }
       }
     }
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) tc::tmem_dealloc(tmem, kTcN);
+  if (warp == 1) tc::tmem_dealloc(tm, kTmN);
+  if (tid == 0 && *abort) raise_status(status, CSA2_STATUS_TIMEOUT);
 }
 
-// The tensor-memory GEMM is used once its operand layout has been checked on
-// the GPU; the mma.sync kernel stays for shapes it does not take.
-constexpr bool kUseTcCompress = true;
+static bool tma_compress_ok(int T, int H, int d, int Di) {
+  return d % kTmN == 0 && H % 16 == 0 && T >= 4 && Di % 4 == 0 && Di <= kTmN && tensor_map_encoder() != nullptr;
+}
 
-static int compress_splits(int M, int N, int Kd) {
-  const int tiles = ((M + kGM - 1) / kGM) * ((N + kGN - 1) / kGN);
-  int splits = 1;
-  // aim for about one wave of 152 SMs while each split keeps >= 1024 of K
-  // (a multiple of the 64-wide K stage of both kernels)
-  while (tiles * splits < 152 && Kd / (splits * 2) >= 1024 && (Kd / (splits * 2)) % 64 == 0) splits *= 2;
-  return splits;
+// Split K only as far as it takes to fill the SMs once.
+static int compress_splits(int B, int G, int N, int Kd) {
+  const int64_t tiles = (int64_t)B * ((G + kTmM - 1) / kTmM) * ((N + kTmN - 1) / kTmN);
+  const int64_t s = std::max<int64_t>(1, kTmSmsTarget / std::max<int64_t>(1, tiles));
+  return (int)std::min<int64_t>(s, std::max(1, Kd / kTmK));
 }
 
 size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out) {
-  const int M = B * (T / 4), N = d + Di, Kd = 4 * H;
-  const int sp = compress_splits(M, N, Kd);
+  const int G = T / 4, M = B * G, N = d + Di, Kd = 4 * H;
+  const int sp = compress_splits(B, G, N, Kd);
   if (n_split_out) *n_split_out = sp;
   return (size_t)sp * M * N * sizeof(float);
 }
@@ -288,16 +297,37 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
                                  cudaStream_t s) {
   const int G = T / 4, M = B * G, N = d + (W_idx ? Di : 0), Kd = 4 * H;
   if (M == 0) return cudaSuccess;
-  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
-  if (kUseTcCompress && (Kd / n_split) % kTcK == 0) {
-    const size_t smem = kTcStages * kTcStageBytes + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (tma_compress_ok(T, H, d, W_idx ? Di : 0)) {
+    // A: [B][G][4H] view of the hidden states; W: [d][4H]; W_idx: [Di][4H]
+    CUtensorMap amap, wmap, imap;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const cuuint64_t adims[3] = {(cuuint64_t)Kd, (cuuint64_t)G, (cuuint64_t)B};
+    const cuuint64_t astr[2] = {(cuuint64_t)Kd * 2, (cuuint64_t)T * H * 2};
+    const cuuint32_t abox[3] = {kTmK, kTmM, 1};
+    const cuuint64_t wdims[2] = {(cuuint64_t)Kd, (cuuint64_t)d};
+    const cuuint64_t wstr[1] = {(cuuint64_t)Kd * 2};
+    const cuuint32_t wbox[2] = {kTmK, kTmN};
+    const cuuint64_t idims[2] = {(cuuint64_t)Kd, (cuuint64_t)(W_idx ? Di : d)};
+    EncodeTiled enc = tensor_map_encoder();
+    if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(hidden), adims, astr, abox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W), wdims, wstr, wbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&imap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W_idx ? W_idx : W), idims, wstr, wbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+    const size_t smem = sizeof(CompressSmem) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_step(k_compress_gemm_tc, grid, dim3(kTcThreads), smem, s, hidden, G, T, H, W, d, W_idx,
-                       W_idx ? Di : 0, M, Kd / n_split, partials, status_word());
+    dim3 grid((N + kTmN - 1) / kTmN, (G + kTmM - 1) / kTmM, B * n_split);
+    return launch_step(k_compress_gemm_tma, grid, dim3(kTmThreads), smem, s, amap, wmap, imap, G, d, N, M,
+                       Kd / kTmK, n_split, partials, status_word());
   }
-  k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M,
-                                             Kd / n_split, partials);
+  dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
+  k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M, partials);
   return counted(cudaGetLastError());
 }
 

@@ -17,13 +17,12 @@
 // 32 KB stages), warp 1 allocates tensor memory and issues the MMAs, warps
 // 2..17 are the epilogue (warp w reads lane quarter w % 4 and queries
 // 8 * ((w - 2) / 4) .. +7 of the block).
-#include <cuda.h>   // CUtensorMap and the tensor-map encoder's signature
-
 #include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
+#include "tma.cuh"
 
 namespace csa2 {
 namespace {
@@ -48,14 +47,6 @@ struct GemmSmem {
   uint32_t tmem;
   int abort;
 };
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(tc::smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ bool role_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < (1u << 22); ++i) {
@@ -159,7 +150,7 @@ k_index_scores_gemm(IndexerArgs a, const __grid_constant__ CUtensorMap kmap, int
           for (int h = 0; h < 2; ++h)
             if (pg[h] >= 0)
               for (int kb = 0; kb < 2; ++kb)   // dims 64*kb .. +63 of the page's 64 rows
-                tma_load_2d(sm.ring[st] + kb * 16384 + h * 8192, &kmap, 64 * kb, pg[h] * kPage, &sm.full[st]);
+                tma::load_2d(sm.ring[st] + kb * 16384 + h * 8192, &kmap, 64 * kb, pg[h] * kPage, &sm.full[st]);
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
@@ -242,28 +233,11 @@ k_index_scores_gemm(IndexerArgs a, const __grid_constant__ CUtensorMap kmap, int
   if (tid == 0 && *abort) raise_status(status, CSA2_STATUS_TIMEOUT);
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link to libcuda).
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-EncodeTiled encoder() {
-  static EncodeTiled fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiled>(p);
-  }
-  return fn;
-}
-
 }  // namespace
 
 bool index_scores_gemm_supported(const IndexerArgs& a) {
   return a.dtype == CSA2_BF16 && a.Hi == kGHi && a.Di == kGDi && a.Tq >= kQB && a.n_pages > 0 &&
-         a.n_pages * kPage < ((int64_t)1 << 31) && encoder() != nullptr;
+         a.n_pages * kPage < ((int64_t)1 << 31) && tensor_map_encoder() != nullptr;
 }
 
 cudaError_t launch_index_scores_gemm(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
@@ -274,7 +248,7 @@ cudaError_t launch_index_scores_gemm(const IndexerArgs& a, float* scores, int64_
   const cuuint64_t strides[1] = {(cuuint64_t)kGDi * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)kPage};
   const cuuint32_t estr[2] = {1, 1};
-  if (encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.k), dims, strides, box, estr,
+  if (tensor_map_encoder()(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.k), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;

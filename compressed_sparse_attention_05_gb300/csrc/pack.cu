@@ -6,6 +6,8 @@
 // Bandwidth-bound: every kernel reads and writes each byte once with 16-byte
 // (or 8-byte) accesses.  Built without fast-math: the divisions that decide a
 // code are IEEE fp32 divisions, as the bit-exact contract requires.
+#include <cmath>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -100,7 +102,17 @@ __global__ void k_pack_fp8_window(const float* __restrict__ x, int B, int Tq, in
 
 // RMSNorm + RoPE + MXFP4 pack + paged store of one entry per warp.  Lane l
 // owns channels 16l .. 16l+15 (one MXFP4 group); d <= 512.
+//
+// RoPE angles: position p = 4e + 3 reaches 4M, so the angle p * theta_i can
+// be ~4e6 rad.  The rotation of frequency i is kept as turns per position,
+// g_i = frac(theta_i / 2 pi) in 0.64 fixed point (host, fp64); p * g_i mod
+// 2^64 in integer arithmetic is then the angle's exact fraction of a turn
+// (error <= p * 2^-53 turns), and sincospi of that fraction in [-1, 1) gives
+// sin and cos.  (fp64 is slow on this GPU; fp32 alone would lose the angle.)
 constexpr int kNrpWarps = 4;
+struct RopeTurns {
+  uint64_t g[256];   // r/2 <= 256 frequencies
+};
 
 __global__ void __launch_bounds__(kNrpWarps * 32)
 k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
@@ -108,13 +120,9 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
                  const int32_t* __restrict__ n_rows, const int32_t* __restrict__ page_table,
                  int max_pages, int64_t n_pages, uint8_t* __restrict__ kv_codes,
                  uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
-                 int Di, int idx_dtype, void* idx_k, uint32_t* status) {
+                 int Di, int idx_dtype, void* idx_k, const __grid_constant__ RopeTurns rope, uint32_t* status) {
   __shared__ float row_buf[kNrpWarps][512];
-  __shared__ double inv_freq[256];   // base^(-2i/r), i < r/2 (r <= 512)
-  // the r/2 rotation frequencies once per CTA, in fp64
   pdl_trigger();
-  for (int i = threadIdx.x; i < r / 2; i += blockDim.x) inv_freq[i] = pow((double)rope_base, -2.0 * (double)i / (double)r);
-  __syncthreads();
   pdl_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
@@ -156,7 +164,7 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
   __syncwarp();
   // rotate-half RoPE on channels [d - r, d) at position 4e + 3
   const int half = r / 2;
-  const double pos = 4.0 * (double)e + 3.0;
+  const uint64_t pos = 4ull * (uint64_t)e + 3ull;
   if (has && r > 0) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -164,19 +172,17 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
       if (ch < d - r) continue;
       const bool first = ch < d - half;
       const int pi = first ? ch - (d - r) : ch - (d - half);
-      // angle reduced to [-pi, pi] in fp64 first (positions reach 4M, so the
-      // angle can be ~4e6 rad); sincos then stays on its short path
-      const double ang = pos * inv_freq[pi];
-      const double red = fma(-6.283185307179586, rint(ang * 0.15915494309189535), ang);
-      double sn, cs;
-      sincos(red, &sn, &cs);
-      const double self = (double)row_buf[warp][ch];
+      const uint64_t turns = pos * rope.g[pi];                 // fraction of a turn, mod 2^64
+      const float t = (float)(int64_t)turns * 0x1p-63f;        // angle / pi in [-1, 1)
+      float sn, cs;
+      sincospif(t, &sn, &cs);
+      const float self = row_buf[warp][ch];
       if (first) {
-        const double other = (double)row_buf[warp][ch + half];
-        v[c] = (float)(self * cs - other * sn);
+        const float other = row_buf[warp][ch + half];
+        v[c] = self * cs - other * sn;
       } else {
-        const double other = (double)row_buf[warp][ch - half];
-        v[c] = (float)(other * sn + self * cs);
+        const float other = row_buf[warp][ch - half];
+        v[c] = other * sn + self * cs;
       }
     }
   }
@@ -244,9 +250,16 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
                                   cudaStream_t s) {
   const int64_t rows = (int64_t)B * n_max;
   if (rows == 0) return cudaSuccess;
+  if (r < 0 || r / 2 > 256) return cudaErrorInvalidValue;
+  RopeTurns rope = {};
+  for (int i = 0; i < r / 2; ++i) {   // theta_i = base^(-2i/r) radians per position, as turns
+    const double f = std::pow((double)rope_base, -2.0 * i / (double)r) / (2.0 * 3.14159265358979323846);
+    const double frac = std::ldexp(f - std::floor(f), 64);
+    rope.g[i] = frac >= 18446744073709551616.0 ? 0ull : (uint64_t)frac;
+  }
   return launch_step(k_norm_rope_pack, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
       src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
-      n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, status_word());
+      n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, rope, status_word());
 }
 
 }  // namespace csa2

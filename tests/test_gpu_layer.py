@@ -118,6 +118,27 @@ def test_prefill_small_with_compression():
     assert np.allclose(kk, new["idx_k"], rtol=2e-2, atol=2e-2)
 
 
+def test_prefill_batch2_with_compression():
+    """Two sequences of 602 new tokens (150 entries each; the two trailing
+    tokens make no entry): ragged 128-entry tiles and the batch stride of the
+    compression GEMM, the many-rows Top-K, attention."""
+    wl = WL.Workload(name="prefill_b2_small", seed=5, B=2, t_first=[4096, 2048], n_new=602, H=256,
+                     description="2 sequences x 602 new tokens, hidden 256")
+    g, _ = check_group(wl, [(0, 0), (0, 301), (0, 601), (1, 0), (1, 599), (1, 601)])
+    for b in range(2):
+        st = OL.SequenceState(wl, b)
+        new = st.new_entries()
+        assert len(new["entry_ids"]) == 150
+        ids = torch.from_numpy(new["entry_ids"])
+        slots = g.page_table[b, ids // 64].long().cpu() * 64 + ids % 64
+        codes = g.kv_codes[slots.cuda()].cpu().numpy()
+        scales = g.kv_scales[slots.cuda()].cpu().numpy()
+        assert (scales != new["scales"]).mean() < 0.01
+        assert (codes != new["codes"]).mean() < 0.01
+        kk = g.idx_k[slots.cuda()].float().cpu().double().numpy()
+        assert np.allclose(kk, new["idx_k"], rtol=2e-2, atol=2e-2)
+
+
 def test_hierarchical_group_small():
     wl = WL.hierarchical_1m(B=2, L=4 * 20000 + 2)
     check_group(wl, [(0, 0), (1, 0)])
