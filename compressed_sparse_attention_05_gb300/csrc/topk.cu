@@ -477,7 +477,128 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
     }
   }
   __syncthreads();
-  finish_from_candidates<kTopkThreads>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
+  finish_from_candidates<kTopkThreads, TopkSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
+}
+
+// ---- rows whose histogram is given (decode: built by the scoring kernel) ------------
+// The threshold bin is known before the row is read, so the row's first loads
+// are issued first and the bin is located while they are in flight; every
+// entry is then compared as a float with the bin's edges: above the bin ->
+// selection bit, inside -> candidate.  The finish is k_topk's.
+constexpr int kHistBatch = 32;   // row elements per thread in flight
+
+template <bool kVec>
+__device__ __forceinline__ int hb_index(int j0, int tid, int u) {
+  return kVec ? j0 + 4 * ((u >> 2) * kTopkThreads + tid) + (u & 3) : j0 + u * kTopkThreads + tid;
+}
+template <bool kVec>
+__device__ __forceinline__ void load_hb(const float* __restrict__ s, int n, int j0, int tid, float (&x)[kHistBatch]) {
+  if (kVec) {
+#pragma unroll
+    for (int u = 0; u < kHistBatch / 4; ++u) {
+      const int j = hb_index<true>(j0, tid, 4 * u);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (j + 3 < n) {
+        f = *reinterpret_cast<const float4*>(s + j);
+      } else if (j < n) {
+        f.x = s[j];
+        if (j + 1 < n) f.y = s[j + 1];
+        if (j + 2 < n) f.z = s[j + 2];
+      }
+      x[4 * u] = f.x; x[4 * u + 1] = f.y; x[4 * u + 2] = f.z; x[4 * u + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kHistBatch; ++u) {
+      const int j = hb_index<false>(j0, tid, u);
+      x[u] = j < n ? s[j] : 0.f;
+    }
+  }
+}
+// The float whose order_key is `key` (key > 0).
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kTopkThreads, 1)
+k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+            int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int64_t row = blockIdx.x;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);   // <= stride <= kBitmapMax (checked by the launcher)
+  const int kk = min(k, n);
+  int32_t* out = out_idx + row * (int64_t)k;
+  const int tid = threadIdx.x, lane = tid & 31;
+
+  for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
+  if (tid == 0) out_cnt[row] = kk;
+  if (kk == 0) return;
+  if (kk == n) {
+    for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
+    return;
+  }
+  float x[kHistBatch];
+  load_hb<kVec>(s, n, 0, tid, x);   // in flight while the bin is located
+  const int words = (n + 31) / 32;
+  for (int i = tid; i < words; i += kTopkThreads) {
+    sm.sel_bits[i] = 0;
+    sm.tie_bits[i] = 0;
+  }
+  if (tid == 0) sm.nC = 0;
+  for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
+  __syncthreads();
+  int above;
+  const int bstar = find_digit_t<kTopkThreads>(sm.hist, 2048, kk, sm.warp_tot, &above);
+  const int need = kk - above;
+  if ((int)sm.hist[bstar] > kCandCap) {
+    radix_whole_row<kTopkThreads>(sm, s, n, kk, bstar, need, out, remap, row);
+    return;
+  }
+  const float f_lo = bstar == 0 ? -INFINITY : key_float((uint32_t)bstar << 21);
+  const float f_hi = bstar == 2047 ? __uint_as_float(0x7FFFFFFFu) : key_float((uint32_t)(bstar + 1) << 21);   // NaN: none above
+  for (int j0 = 0; j0 < n; j0 += kTopkThreads * kHistBatch) {
+    if (j0 > 0) load_hb<kVec>(s, n, j0, tid, x);
+    uint32_t cm = 0;
+#pragma unroll
+    for (int u = 0; u < kHistBatch; ++u) {
+      const int j = hb_index<kVec>(j0, tid, u);
+      if (j < n) {
+        if (x[u] >= f_hi) red_or_shared(&sm.sel_bits[j >> 5], 1u << (j & 31));
+        else if (x[u] >= f_lo) cm |= 1u << u;
+      }
+    }
+    const int c = __popc(cm);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+    if (wtot) {
+      int base = 0;
+      if (lane == 31) base = atomicAdd(&sm.nC, wtot);
+      base = __shfl_sync(0xffffffffu, base, 31);
+      int pos = base + incl - c;
+#pragma unroll
+      for (int u = 0; u < kHistBatch; ++u) {
+        if ((cm >> u) & 1u) {
+          if (pos < kCandCap) {
+            sm.ckey[pos] = order_key(x[u]);
+            sm.cidx[pos] = hb_index<kVec>(j0, tid, u);
+          }
+          ++pos;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  finish_from_candidates<kTopkThreads, TopkSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
 }
 
 // ---- many short rows (prefill: one row per query token) ------------------------------
@@ -539,10 +660,6 @@ __device__ __forceinline__ void load_batch(const float* __restrict__ s, int n, i
     }
   }
 }
-// The float whose order_key is `key` (key > 0).
-__device__ __forceinline__ float key_float(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 
 // Appends the batch's entries at or above f_lo (all of them with take_all) to
 // the candidates (one atomic per warp) and adds their keys to the histogram.
@@ -597,7 +714,7 @@ k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int 
   const int n = row_valid(v, row, stride);   // <= stride <= kShortMaxN (checked by the launcher)
   const int kk = min(k, n);
   int32_t* out = out_idx + row * (int64_t)k;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
 
   for (int j = kk + tid; j < k; j += NT) out[j] = -1;
   if (tid == 0) out_cnt[row] = kk;
@@ -823,7 +940,7 @@ k_topk_finish(const float* __restrict__ scores, int64_t stride, ValidSpec v, int
     sm.cidx[i] = cand_idx[row * kCandCap + i];
   }
   __syncthreads();
-  finish_from_candidates<kTopkThreads>(sm, n, kk, bstar, need, nC, out, remap, row);
+  finish_from_candidates<kTopkThreads, TopkSmem, true>(sm, n, kk, bstar, need, nC, out, remap, row);
 }
 
 // 2048-bin key histograms of given score rows (for the split path on a given array).
@@ -935,6 +1052,19 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     if (e != cudaSuccess) return e;
     return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
                        out_idx, out_cnt, remap);
+  }
+  if (hist && rows <= sms && stride <= kBitmapMax) {   // histogram given: bin located while the row loads
+    const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
+    if (vec) {
+      e = cudaFuncSetAttribute(k_topk_hist<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_step(k_topk_hist<true>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k,
+                         out_idx, out_cnt, remap, hist, hist_stride);
+    }
+    e = cudaFuncSetAttribute(k_topk_hist<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_step(k_topk_hist<false>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k,
+                       out_idx, out_cnt, remap, hist, hist_stride);
   }
   if (rows <= sms) {   // one wave of rows: latency counts, occupancy does not
     e = cudaFuncSetAttribute(k_topk<32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
