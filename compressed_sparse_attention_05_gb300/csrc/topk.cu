@@ -31,6 +31,11 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The float whose order_key is `key` (key > 0).
+__device__ __forceinline__ float key_float(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 __device__ __forceinline__ int row_valid(const ValidSpec& v, int64_t row, int64_t stride) {
   int64_t n;
   if (v.n_valid) {
@@ -515,10 +520,6 @@ __device__ __forceinline__ void load_hb(const float* __restrict__ s, int n, int 
     }
   }
 }
-// The float whose order_key is `key` (key > 0).
-__device__ __forceinline__ float key_float(uint32_t key) {
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 
 template <bool kVec>
 __global__ void __launch_bounds__(kTopkThreads, 1)
@@ -856,45 +857,45 @@ k_topk_collect(const float* __restrict__ scores, int64_t stride, ValidSpec v, in
   pdl_wait();
   __shared__ uint32_t shist[2048];
   __shared__ int warp_tot[kCollectThreads / 32];
+  constexpr int kPer = kCollectChunk / kCollectThreads;   // 16 entries per thread
   const int64_t row = blockIdx.y;
   const float* s = scores + row * stride;
   const int n = row_valid(v, row, stride);
   const int kk = min(k, n);
   const int c0 = blockIdx.x * kCollectChunk;
   if (kk == 0 || kk == n || c0 >= n || n > kBitmapMax) return;
+  const int c1 = min(n, c0 + kCollectChunk);
+  const int tid = threadIdx.x, lane = tid & 31;
+  // the chunk's loads are in flight while the threshold bin is located
+  float vv[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int j = c0 + u * kCollectThreads + tid;
+    vv[u] = j < c1 ? s[j] : 0.f;
+  }
   int bstar, above;
   locate_bin<kCollectThreads>(shist, warp_tot, s, n, kk, hist_in + row * hist_stride, &bstar, &above);
   if ((int)shist[bstar] > kCandCap) return;       // the finish kernel takes the whole-row path
-  const int c1 = min(n, c0 + kCollectChunk);
-  const int tid = threadIdx.x, lane = tid & 31;
-  for (int j0 = c0; j0 < c1; j0 += kCollectThreads * kBatch) {
-    float vv[kBatch];
+  // the bin's edges as floats: above -> selection word bit, inside -> candidate
+  const float f_lo = bstar == 0 ? -INFINITY : key_float((uint32_t)bstar << 21);
+  const float f_hi = bstar == 2047 ? __uint_as_float(0x7FFFFFFFu) : key_float((uint32_t)(bstar + 1) << 21);
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kCollectThreads + tid;
-      vv[u] = j < c1 ? s[j] : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kCollectThreads + tid;
-      uint32_t key = 0, bin = 0;
-      if (j < c1) {
-        key = order_key(vv[u]);
-        bin = key >> 21;
-      }
-      const uint32_t word = __ballot_sync(0xffffffffu, j < c1 && bin > (uint32_t)bstar);
-      if (lane == 0 && j < c1) sel_words[row * words_stride + (j >> 5)] = word;
-      const bool cand = j < c1 && bin == (uint32_t)bstar;
-      const uint32_t m = __ballot_sync(0xffffffffu, cand);
-      if (m) {
-        int base = 0;
-        if (lane == __ffs(m) - 1) base = atomicAdd(&cand_count[row], __popc(m));
-        base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
-        const int pos = base + __popc(m & ((1u << lane) - 1));
-        if (cand && pos < kCandCap) {
-          cand_key[row * kCandCap + pos] = key;
-          cand_idx[row * kCandCap + pos] = j;
-        }
+  for (int u = 0; u < kPer; ++u) {
+    const int j = c0 + u * kCollectThreads + tid;   // a warp covers one aligned 32-entry word
+    const bool in = j < c1;
+    const bool sel = in && vv[u] >= f_hi;
+    const uint32_t word = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0 && in) sel_words[row * words_stride + (j >> 5)] = word;
+    const bool cand = in && !sel && vv[u] >= f_lo;
+    const uint32_t m = __ballot_sync(0xffffffffu, cand);
+    if (m) {
+      int base = 0;
+      if (lane == __ffs(m) - 1) base = atomicAdd(&cand_count[row], __popc(m));
+      base = __shfl_sync(0xffffffffu, base, __ffs(m) - 1);
+      const int pos = base + __popc(m & ((1u << lane) - 1));
+      if (cand && pos < kCandCap) {
+        cand_key[row * kCandCap + pos] = order_key(vv[u]);
+        cand_idx[row * kCandCap + pos] = j;
       }
     }
   }
