@@ -136,7 +136,7 @@ static bool use_split_topk(int64_t rows, int32_t max_entries) {
 }
 
 struct IndexWs {
-  size_t scores_off, bm_off, nvalid_off, hist_off, split_off, total;
+  size_t scores_off, bm_off, nvalid_off, hist_off, bmhist_off, split_off, total;
   int64_t s_stride, bm_stride;
 };
 static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
@@ -152,7 +152,8 @@ static IndexWs index_ws_layout(const csa2_dims* dm, int32_t max_entries) {
   L.bm_off = round_up(L.scores_off + (size_t)(rows * L.s_stride) * 4, 256);
   L.nvalid_off = round_up(L.bm_off + (size_t)(rows * L.bm_stride) * 4, 256);
   L.hist_off = round_up(L.nvalid_off + (size_t)rows * 4, 256);
-  L.split_off = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
+  L.bmhist_off = round_up(L.hist_off + (size_t)rows * kHistBins * 4, 256);
+  L.split_off = round_up(L.bmhist_off + (dm->n_pool_blocks > 0 ? (size_t)rows * kHistBins * 4 : 0), 256);
   const size_t split = use_split_topk(rows, max_entries) ? topk_split_scratch_bytes(rows, L.s_stride) : 0;
   L.total = round_up(L.split_off + split, 256);
   return L;
@@ -399,13 +400,18 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   float* bm = reinterpret_cast<float*>(base + L.bm_off);
   int32_t* nvalid = reinterpret_cast<int32_t*>(base + L.nvalid_off);
   uint32_t* hist = reinterpret_cast<uint32_t*>(base + L.hist_off);
+  uint32_t* bm_hist = (out_pool && dm->n_pool_blocks > 0) ? reinterpret_cast<uint32_t*>(base + L.bmhist_off) : nullptr;
   IndexerArgs a = indexer_args(dm, c, idx_q, w, q_pos);
   a.max_entries = max_entries;
   if (!reindex) {
     // the many-query GEMM path builds no histogram: the Top-K kernel then builds each row's
     if (index_scores_gemm_supported(a)) hist = nullptr;
     if (hist) LAUNCH(cudaMemsetAsync(hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
-    LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s),
+    if (!hist) bm_hist = nullptr;
+    if (bm_hist) LAUNCH(cudaMemsetAsync(bm_hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
+    bool bm_built = false;
+    LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s,
+                               bm_hist, &bm_built),
            "index_scores");
     ValidSpec v{nullptr, c->n_entries, q_pos, dm->Tq, 1, max_entries};
     if (hist && use_split_topk(rows, max_entries))
@@ -419,7 +425,7 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
     if (out_pool) {
       ValidSpec vb{nullptr, c->n_entries, q_pos, dm->Tq, 8, max_entries};
       LAUNCH(launch_topk(bm, rows, L.bm_stride, vb, dm->n_pool_blocks, out_pool, out_pool_cnt,
-                         Remap{nullptr, 0, 8}, nullptr, 0, s),
+                         Remap{nullptr, 0, 8}, bm_built ? bm_hist : nullptr, bm_built ? kHistBins : 0, s),
              "block_pool");
     }
   } else {

@@ -267,13 +267,15 @@ template <int NT>
 __global__ void __launch_bounds__(kScanThreads)
 k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, float* __restrict__ scores,
                    int64_t stride, float* __restrict__ blockmax, int64_t bm_stride, uint32_t* __restrict__ hist,
-                   uint32_t* status) {
+                   uint32_t* __restrict__ bm_hist, uint32_t* status) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ ScanShared ss;
   pdl_trigger();
   pdl_wait();
   unsigned char* ring = smem_raw;                                   // kScanStages pages
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem_raw + kScanStages * kPageBytes);
+  // block-maxima histogram of the (one) query row, after the score histogram
+  uint32_t* sbm = shist + (hist ? kHistBins : 0);
   int b, p0, p1, i0, i1;
   if (flat_slots > 0) {          // one query per row
     if (!flat_assign(a, flat_slots, b, p0, p1)) return;
@@ -303,6 +305,8 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
   }
   if (hist)
     for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) shist[i] = 0;
+  if (bm_hist)   // one query row per CTA on this path (checked by the launcher)
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sbm[i] = 0;
   __syncthreads();
   volatile int* abort = &ss.abort;
 
@@ -401,6 +405,10 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
             }
             if (lane == 0) blockmax[row * bm_stride + e0 / 8] = m0;
             if (lane == 1 && e0 + 8 < nv) blockmax[row * bm_stride + e0 / 8 + 1] = m1;
+            if (bm_hist) {   // the blocks with a visible entry, as for the scores
+              if (lane == 0 && e0 < nv) atomicAdd(&sbm[score_key(m0) >> 21], 1u);
+              if (lane == 1 && e0 + 8 < nv) atomicAdd(&sbm[score_key(m1) >> 21], 1u);
+            }
           }
         }
       }
@@ -414,6 +422,12 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
     for (int i = threadIdx.x; i < (i1 - i0) * kHistBins; i += blockDim.x) {
       const uint32_t c = shist[i];
       if (c) atomicAdd(&hist[((int64_t)b * a.Tq + i0 + i / kHistBins) * kHistBins + (i % kHistBins)], c);
+    }
+  }
+  if (bm_hist) {
+    for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) {
+      const uint32_t c = sbm[i];
+      if (c) atomicAdd(&bm_hist[((int64_t)b * a.Tq + i0) * kHistBins + i], c);
     }
   }
 }
@@ -430,7 +444,8 @@ static int num_sms() {
 
 template <int NT>
 static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
-                                     int64_t bm_stride, int max_entries, uint32_t* hist, cudaStream_t s) {
+                                     int64_t bm_stride, int max_entries, uint32_t* hist, uint32_t* bm_hist,
+                                     cudaStream_t s) {
   const int QG = a.Tq >= kHistMaxQG ? kHistMaxQG : a.Tq;
   const int q_groups = (a.Tq + QG - 1) / QG;
   const int max_pages_vis = (max_entries + kPage - 1) / kPage;
@@ -440,7 +455,9 @@ static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_
   per_seq = per_seq < 1 ? 1 : per_seq;
   int ppc = (max_pages_vis + per_seq - 1) / per_seq;
   ppc = ppc < 1 ? 1 : ppc;
-  const size_t smem = (size_t)kScanStages * kPageBytes + (hist ? (size_t)QG * kHistBins * 4 : 0);
+  if (a.Tq != 1 || !blockmax) bm_hist = nullptr;   // one query row per CTA only
+  const size_t smem = (size_t)kScanStages * kPageBytes + (hist ? (size_t)QG * kHistBins * 4 : 0) +
+                      (bm_hist ? (size_t)kHistBins * 4 : 0);
   cudaError_t e = cudaFuncSetAttribute(k_index_scan_pages<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.Tq == 1) {
@@ -451,11 +468,11 @@ static cudaError_t launch_scan_pages(const IndexerArgs& a, float* scores, int64_
     const int slots = per_sm * num_sms();
     const int grid = slots > a.B ? slots : a.B + 1;
     return launch_step(k_index_scan_pages<NT>, dim3(grid), dim3(kScanThreads), smem, s, a, 1, 0, grid, scores, stride,
-                       blockmax, bm_stride, hist, status_word());
+                       blockmax, bm_stride, hist, bm_hist, status_word());
   }
   dim3 grid((max_pages_vis + ppc - 1) / ppc, q_groups, a.B);
   return launch_step(k_index_scan_pages<NT>, grid, dim3(kScanThreads), smem, s, a, QG, ppc, 0, scores, stride,
-                     blockmax, bm_stride, hist, status_word());
+                     blockmax, bm_stride, hist, bm_hist, status_word());
 }
 
 // Histogram of already-written scores (the generic scoring path).
@@ -619,7 +636,9 @@ static cudaError_t launch_pool_mma(const IndexerArgs& a, const int32_t* pool, co
   } while (0)
 
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
-                                int64_t bm_stride, int block, int max_entries, uint32_t* hist, cudaStream_t s) {
+                                int64_t bm_stride, int block, int max_entries, uint32_t* hist, cudaStream_t s,
+                                uint32_t* bm_hist, bool* bm_hist_built) {
+  if (bm_hist_built) *bm_hist_built = false;
   if ((int64_t)a.B * a.Tq == 0 || max_entries == 0) return cudaSuccess;
   if (block == 8 && index_scores_gemm_supported(a)) {
     cudaError_t e = launch_index_scores_gemm(a, scores, stride, blockmax, bm_stride, max_entries, s);
@@ -629,8 +648,9 @@ cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t str
     return counted(cudaGetLastError());
   }
   if (mma_path(a) && block == 8 && a.Di == 128) {
-    if (a.Hi > 8) return launch_scan_pages<2>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
-    return launch_scan_pages<1>(a, scores, stride, blockmax, bm_stride, max_entries, hist, s);
+    if (bm_hist_built) *bm_hist_built = bm_hist && a.Tq == 1 && blockmax;
+    if (a.Hi > 8) return launch_scan_pages<2>(a, scores, stride, blockmax, bm_stride, max_entries, hist, bm_hist, s);
+    return launch_scan_pages<1>(a, scores, stride, blockmax, bm_stride, max_entries, hist, bm_hist, s);
   }
   if (mma_path(a) && block == 8) {
     CSA2_DISPATCH_MMA(launch_full_mma, a, scores, stride, blockmax, bm_stride, max_entries, hist, s);

@@ -94,9 +94,12 @@ struct IndexerArgs {
 };
 // Full: scores[row][j] for visible j; blockmax (nullable) per `block` entries;
 // hist (nullable, zeroed by the caller): per-row 2048-bin key histogram for launch_topk.
+// bm_hist (nullable, zeroed by the caller): the same for the block maxima, built only
+// by the one-query-per-row page scan; *bm_hist_built says whether it was.
 cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t stride,
                                 float* blockmax, int64_t bm_stride, int block, int max_entries,
-                                uint32_t* hist, cudaStream_t s);
+                                uint32_t* hist, cudaStream_t s, uint32_t* bm_hist = nullptr,
+                                bool* bm_hist_built = nullptr);
 // ---- indexer_tc.cu: many query tokens per sequence (prefill) as a tcgen05 GEMM
 // (bf16 keys, Hi = 8, Di = 128, Tq >= 32).  Scores and block maxima as above;
 // builds no histogram (the Top-K kernel builds its own).

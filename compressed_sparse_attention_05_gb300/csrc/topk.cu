@@ -485,11 +485,14 @@ k_topk(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int
   finish_from_candidates<kTopkThreads, TopkSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
 }
 
-// ---- rows whose histogram is given (decode: built by the scoring kernel) ------------
-// The threshold bin is known before the row is read, so the row's first loads
-// are issued first and the bin is located while they are in flight; every
-// entry is then compared as a float with the bin's edges: above the bin ->
-// selection bit, inside -> candidate.  The finish is k_topk's.
+// ---- one row per CTA, histogram given or row in registers ----------------------------
+// When the scoring kernel built the row's histogram (decode) the threshold bin
+// is known before the row is read: the row's first loads are issued first and
+// the bin is located while they are in flight.  Without one, a row of at most
+// 32,768 entries is held in registers whole (32 entries per thread) and its
+// histogram built from them.  Every entry is then compared as a float with the
+// bin's edges: above the bin -> selection bit, inside -> candidate; the finish
+// is k_topk's.
 constexpr int kHistBatch = 32;   // row elements per thread in flight
 
 template <bool kVec>
@@ -551,7 +554,15 @@ k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k
     sm.tie_bits[i] = 0;
   }
   if (tid == 0) sm.nC = 0;
-  for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
+  if (hist_in) {
+    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
+  } else {   // n <= kTopkThreads * kHistBatch (checked by the launcher): the whole row is in x
+    for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kHistBatch; ++u)
+      warp_hist_add(sm.hist, hb_index<kVec>(0, tid, u) < n ? order_key(x[u]) >> 21 : 0xFFFFFFFFu, 2048);
+  }
   __syncthreads();
   int above;
   const int bstar = find_digit_t<kTopkThreads>(sm.hist, 2048, kk, sm.warp_tot, &above);
@@ -1054,7 +1065,7 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
                        out_idx, out_cnt, remap);
   }
-  if (hist && rows <= sms && stride <= kBitmapMax) {   // histogram given: bin located while the row loads
+  if (rows <= sms && (hist ? stride <= kBitmapMax : stride <= (int64_t)kTopkThreads * kHistBatch)) {
     const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
     if (vec) {
       e = cudaFuncSetAttribute(k_topk_hist<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
