@@ -385,20 +385,25 @@ def step_roofline(wl, alg, ms, peaks):
 # ---------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample
 
-def cpu_baseline(workload, seconds):
+def cpu_baseline(workload, seconds, ref_steps=0):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
     cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-worker", "--workload", workload,
-           "--cpu-seconds", str(seconds)]
+           "--cpu-seconds", str(seconds), "--ref-steps", str(ref_steps)]
     r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 20 * seconds))
     if r.returncode != 0:
         return {"error": r.stderr[-500:]}
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_worker(workload, seconds):
+def cpu_worker(workload, seconds, ref_steps=0):
     """Times the oracle's arithmetic for whole query tokens of the workload (inputs and
-    cached state prepared outside the timer), single-threaded."""
+    cached state prepared outside the timer), single-threaded.
+
+    ref_steps > 0 (the reference arm): `seconds` is shared out over ref_steps timed
+    steps; each step runs whole layers of query tokens (in schedule order, at least
+    one layer) until its slice is used, so the run stays bounded whatever the
+    step count; the per-step and aggregate throughputs are reported."""
     import numpy as np
     import torch
 
@@ -434,36 +439,63 @@ def cpu_worker(workload, seconds):
         c, s = st.packed_rows(cand)
         prepared.append((nv, qs, Qs, win_lat, cand, c, s))
 
-    def one_token(nv, qs, Qs, win_lat, cand, c, s):
-        prev = None
-        pool_t = None
-        for l, mode in enumerate(wl.layers):
-            if mode == "F":
-                sc = I.index_scores(qs[l][0], qs[l][1], Kall[:nv])
-                idx = I.topk(sc, wl.K)
-                if wl.hierarchical:
-                    pool_t = I.block_pool(sc, wl.pool_blocks, wl.pool_block)
-            elif mode == "X":
-                pos = I.pool_positions(pool_t, nv, wl.pool_block)
-                idx = pos[I.topk(I.index_scores(qs[l][0], qs[l][1], Kall[pos]), wl.K)]
-            else:
-                idx = prev
-            prev = idx
-            rows = np.searchsorted(cand, idx)
-            kv = F.mxfp4_unpack(c[rows], s[rows])
-            wc, ws = F.fp8_pack(win_lat[l])
-            A.sparse_attention(Qs[l], kv, F.fp8_unpack_bf16(wc, ws), tau)
+    def one_layer(l, state, nv, qs, Qs, win_lat, cand, c, s):
+        """Layer l of one query token; state carries the previous layer's indices and the pool."""
+        mode = wl.layers[l]
+        if mode == "F":
+            sc = I.index_scores(qs[l][0], qs[l][1], Kall[:nv])
+            idx = I.topk(sc, wl.K)
+            if wl.hierarchical:
+                state["pool"] = I.block_pool(sc, wl.pool_blocks, wl.pool_block)
+        elif mode == "X":
+            pos = I.pool_positions(state["pool"], nv, wl.pool_block)
+            idx = pos[I.topk(I.index_scores(qs[l][0], qs[l][1], Kall[pos]), wl.K)]
+        else:
+            idx = state["prev"]
+        state["prev"] = idx
+        rows = np.searchsorted(cand, idx)
+        kv = F.mxfp4_unpack(c[rows], s[rows])
+        wc, ws = F.fp8_pack(win_lat[l])
+        A.sparse_attention(Qs[l], kv, F.fp8_unpack_bf16(wc, ws), tau)
 
-    t_tot, tokens = 0.0, 0
-    while t_tot < seconds:
-        for p in prepared:
+    L = len(wl.layers)
+    unit = [0]   # (token, layer) units run so far, in schedule order
+    state = {}
+
+    def run_units(slice_s):
+        """Whole layers, in order, until slice_s seconds are used (at least one)."""
+        t, n = 0.0, 0
+        while n == 0 or t < slice_s:
+            k = unit[0]
+            l = k % L
+            if l == 0:
+                state.clear()
+            p = prepared[(k // L) % len(prepared)]
             t0 = time.perf_counter()
-            one_token(*p)
-            t_tot += time.perf_counter() - t0
-            tokens += 1
-    per_token = t_tot / max(tokens, 1)
+            one_layer(l, state, *p)
+            t += time.perf_counter() - t0
+            n += 1
+            unit[0] += 1
+        return t, n
+
+    step_tokens = []   # (seconds, tokens) of every reference step
+    if ref_steps > 0:
+        slice_s = seconds / ref_steps
+        for _ in range(ref_steps):
+            t, n = run_units(slice_s)
+            step_tokens.append((t, n / L))
+        t_tot = sum(t for t, _ in step_tokens)
+        tokens = sum(n for _, n in step_tokens)
+    else:
+        t_tot, tokens = 0.0, 0
+        while t_tot < seconds:
+            t, n = run_units(seconds - t_tot)
+            t_tot += t
+            tokens += n / L
+    per_token = t_tot / max(tokens, 1e-9)
     # prefill: the step also compresses the chunk; time the oracle's compression once
     extra = ""
+    t_comp = 0.0
     if wl.H is not None:
         from oracle import compress as Cm
         st = OL.SequenceState(wl, 0)
@@ -473,35 +505,42 @@ def cpu_worker(workload, seconds):
         t0 = time.perf_counter()
         Cm.compress_pack(hid, W, st.gamma, wl.eps, wl.r, wl.rope_base, st.n_before, W_idx=Wi)
         t_comp = time.perf_counter() - t0
-        step_s = t_comp + per_token * wl.Tq
         extra = f"; compression of the {wl.n_new}-token chunk timed once ({t_comp:.2f} s)"
-    else:
-        step_s = per_token * wl.Tq * wl.B
-    value = wl.B * wl.Tq / step_s
-    print(json.dumps({"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                      "sample": f"{tokens} query tokens of {wl.name} through all {len(wl.layers)} layer(s), "
-                                f"{t_tot:.1f} s of single-thread float64 numpy, scaled to the "
-                                f"{wl.B * wl.Tq}-token step{extra}",
-                      "seconds_per_token": per_token}))
+
+    def step_value(sec_per_token):
+        step_s = t_comp + sec_per_token * wl.Tq * wl.B
+        return wl.B * wl.Tq / step_s
+
+    value = step_value(per_token)
+    out = {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{tokens:.2f} query tokens of {wl.name} through all {L} layer(s) (whole layers, in "
+                     f"schedule order), {t_tot:.1f} s of single-thread float64 numpy, scaled to the "
+                     f"{wl.B * wl.Tq}-token step{extra}",
+           "seconds_per_token": per_token}
+    if ref_steps > 0:
+        out["step_values"] = [step_value(t / n) for t, n in step_tokens]
+    print(json.dumps(out))
 
 
 # ---------------------------------------------------------------------------------
 # reference arm: the oracle as it stands, timed on the host cores
 
 def run_reference(args, rank, world):
+    """The oracle as the reference arm: one worker process times warmup + steps
+    steps, each a slice of a fixed CPU budget (--ref-seconds in all), so the run
+    is bounded whatever the step count; value = the timed steps' aggregate
+    throughput (tokens over seconds)."""
     if rank != 0:
         return
-    steps = []
-    last = None
-    for k in range(args.warmup + args.steps):
-        r = cpu_baseline(args.workload, args.ref_seconds)
-        if "error" in r:
-            print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " + r["error"][-200:]}))
-            return
-        if k >= args.warmup:
-            steps.append(r["value"])
-        last = r
-    value = statistics.median(steps)
+    n = args.warmup + args.steps
+    r = cpu_baseline(args.workload, args.ref_seconds, ref_steps=n)
+    if "error" in r:
+        print(json.dumps({"impl": "reference", "unavailable": "oracle run failed: " + r["error"][-200:]}))
+        return
+    timed = r["step_values"][args.warmup:]
+    # aggregate over the timed steps: total tokens / total seconds (harmonic mean of the step rates)
+    value = len(timed) / sum(1.0 / v for v in timed) if timed else r["value"]
+    last = r
     wl = make_workload(args.workload)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -522,12 +561,14 @@ def main():
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "hierarchical", "ragged"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--ref-seconds", type=float, default=5.0)
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="CPU budget of the whole reference run, shared out over warmup + steps")
+    ap.add_argument("--ref-steps", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-worker", action="store_true")
     args = ap.parse_args()
     if args.cpu_worker:
-        cpu_worker(args.workload, args.cpu_seconds)
+        cpu_worker(args.workload, args.cpu_seconds, args.ref_steps)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
