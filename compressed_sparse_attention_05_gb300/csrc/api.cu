@@ -433,7 +433,7 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
            "index_scores_pool");
     ValidSpec v{nvalid, nullptr, nullptr, 1, 1, 0};
     LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt,
-                       Remap{pool, dm->n_pool_blocks, 8}, nullptr, 0, s),
+                       Remap{pool, dm->n_pool_blocks, 8}, nullptr, 0, s, (int64_t)dm->n_pool_blocks * 8),
            "reindex_topk");
   }
   return CSA2_OK;

@@ -133,9 +133,12 @@ struct Remap {
 };
 // hist (nullable): per-row 2048-bin histogram of the top 11 bits of the
 // order-preserving score keys of the valid columns (built by the scoring kernel).
+// max_n (> 0): a bound on every row's valid count below the stride (the row
+// is then read as if it were that long; valid counts above it are reported
+// as CSA2_STATUS_BAD_COUNT and clamped).
 cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
                         int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
-                        int64_t hist_stride, cudaStream_t s);
+                        int64_t hist_stride, cudaStream_t s, int64_t max_n = 0);
 // Split Top-K for few rows: many CTAs per row collect, one CTA per row
 // finishes.  Needs the row histograms and topk_split_scratch_bytes of scratch.
 size_t topk_split_scratch_bytes(int64_t rows, int64_t stride);

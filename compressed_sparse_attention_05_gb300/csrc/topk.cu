@@ -527,14 +527,19 @@ __device__ __forceinline__ void load_hb(const float* __restrict__ s, int n, int 
 template <bool kVec>
 __global__ void __launch_bounds__(kTopkThreads, 1)
 k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
-            int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride) {
+            int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in, int64_t hist_stride,
+            uint32_t* status) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   const int64_t row = blockIdx.x;
   const float* s = scores + row * stride;
-  const int n = row_valid(v, row, stride);   // <= stride <= kBitmapMax (checked by the launcher)
+  int n = row_valid(v, row, stride);   // <= kBitmapMax, or <= the register capacity without hist_in
+  if (!hist_in && n > kTopkThreads * kHistBatch) {   // the launcher's bound on the valid counts was wrong
+    if (threadIdx.x == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    n = kTopkThreads * kHistBatch;
+  }
   const int kk = min(k, n);
   int32_t* out = out_idx + row * (int64_t)k;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -1044,8 +1049,9 @@ __global__ void k_block_max(const float* __restrict__ scores, int64_t stride, Va
 
 cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, ValidSpec v, int k,
                         int32_t* out_idx, int32_t* out_cnt, Remap remap, const uint32_t* hist,
-                        int64_t hist_stride, cudaStream_t s) {
+                        int64_t hist_stride, cudaStream_t s, int64_t max_n) {
   if (rows == 0) return cudaSuccess;
+  const int64_t span = (max_n > 0 && max_n < stride) ? max_n : stride;   // longest valid row
   const size_t smem = sizeof(TopkSmem);
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1065,18 +1071,18 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
                        out_idx, out_cnt, remap);
   }
-  if (rows <= sms && (hist ? stride <= kBitmapMax : stride <= (int64_t)kTopkThreads * kHistBatch)) {
+  if (rows <= sms && (hist ? span <= kBitmapMax : span <= (int64_t)kTopkThreads * kHistBatch)) {
     const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
     if (vec) {
       e = cudaFuncSetAttribute(k_topk_hist<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       return launch_step(k_topk_hist<true>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k,
-                         out_idx, out_cnt, remap, hist, hist_stride);
+                         out_idx, out_cnt, remap, hist, hist_stride, status_word());
     }
     e = cudaFuncSetAttribute(k_topk_hist<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_step(k_topk_hist<false>, dim3((unsigned)rows), dim3(kTopkThreads), smem, s, scores, stride, v, k,
-                       out_idx, out_cnt, remap, hist, hist_stride);
+                       out_idx, out_cnt, remap, hist, hist_stride, status_word());
   }
   if (rows <= sms) {   // one wave of rows: latency counts, occupancy does not
     e = cudaFuncSetAttribute(k_topk<32, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
