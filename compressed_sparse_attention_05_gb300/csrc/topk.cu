@@ -620,7 +620,7 @@ k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k
 
 // ---- many short rows (prefill: one row per query token) ------------------------------
 // Rows of at most 32,768 entries, many more rows than SMs: a 256-thread CTA
-// per row, four rows per SM, and few instructions per entry.  A sample of the
+// per row, six rows per SM, and few instructions per entry.  A sample of the
 // row (64 spread runs of 16 entries) gives a lower bound for the K-th key: the
 // bin of the sample's r-th largest key, r = 1.5 times the sample's expected
 // share of the Top-K plus 8.  One pass over the row then compares every entry with
@@ -632,8 +632,8 @@ k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k
 // passes over the whole row instead.
 constexpr int kShortThreads = 256;
 constexpr int kShortMaxN = 32768;
-constexpr int kShortCap = 4096;     // candidates kept in shared memory
-constexpr int kShortBatch = 16;     // row elements per thread loaded before any is used
+constexpr int kShortCap = 2048;     // candidates kept in shared memory
+constexpr int kShortBatch = 8;      // row elements per thread loaded before any is used
 constexpr int kSample = 1024;       // 64 runs of 16 entries
 
 struct TopkShortSmem {
@@ -717,7 +717,7 @@ __device__ __forceinline__ void collect_batch(TopkShortSmem& sm, const float (&x
 }
 
 template <bool kVec>
-__global__ void __launch_bounds__(kShortThreads, 4)
+__global__ void __launch_bounds__(kShortThreads, 6)
 k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
              int32_t* __restrict__ out_cnt, Remap remap) {
   pdl_trigger();
