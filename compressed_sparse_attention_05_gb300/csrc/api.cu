@@ -328,6 +328,11 @@ int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32
     uint32_t* hist = static_cast<uint32_t*>(ws);
     char* split = static_cast<char*>(ws) + round_up((size_t)rows * kHistBins * 4, 256);
     LAUNCH(launch_row_hist(scores, rows, stride, v, hist, s), "row_hist");
+    if (stride <= 32768) {   // rows the one-pass kernels take whole (a cluster or a CTA per row)
+      LAUNCH(launch_topk(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins, s),
+             "topk");
+      return CSA2_OK;
+    }
     LAUNCH(launch_topk_split(scores, rows, stride, v, k, out_idx, out_cnt, Remap{nullptr, 0, 8}, hist, kHistBins,
                              split, s),
            "topk_split");

@@ -618,6 +618,159 @@ k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k
   finish_from_candidates<kTopkThreads, TopkSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kCandCap), out, remap, row);
 }
 
+// ---- few rows with a given histogram, each spread over a cluster -------------------------
+// Decode: 32 rows of 32,768 scores would keep 32 SMs busy.  A cluster of
+// kTopkRanks CTAs takes one row: every rank locates the threshold bin from
+// the row's histogram itself, classifies its quarter of the row (float
+// compares with the bin's edges) and writes the selection bits and the
+// threshold bin's candidates into rank 0's shared memory (distributed
+// shared-memory reductions and stores); rank 0 then finishes as k_topk does.
+constexpr int kTopkRanks = 4;
+constexpr int kClusterMaxN = kTopkRanks * kTopkThreads * 8;   // 8 entries per thread and rank
+constexpr int kClusterCap = 4096;
+
+struct TopkClusterSmem {
+  uint32_t hist[2048];
+  uint32_t hist2[256];
+  int warp_tot[kTopkWarps];
+  int nC, pad_;
+  uint32_t ckey[kClusterCap];
+  int32_t cidx[kClusterCap];
+  uint32_t sel_bits[kClusterMaxN / 32];
+  uint32_t tie_bits[kClusterMaxN / 32];
+};
+
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {   // this CTA's address in `rank`
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_red_or(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kTopkThreads, 1)
+k_topk_cluster(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
+               int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in,
+               int64_t hist_stride) {
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TopkClusterSmem& sm = *reinterpret_cast<TopkClusterSmem*>(smem_raw);
+  const uint32_t rank = cl_rank();
+  const int64_t row = blockIdx.x / kTopkRanks;
+  const float* s = scores + row * stride;
+  const int n = row_valid(v, row, stride);   // <= stride <= kClusterMaxN (checked by the launcher)
+  const int kk = min(k, n);
+  int32_t* out = out_idx + row * (int64_t)k;
+  const int tid = threadIdx.x, lane = tid & 31;
+  // every rank takes the same early exits: they depend on the row only
+  if (rank == 0) {
+    for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
+    if (tid == 0) out_cnt[row] = kk;
+  }
+  if (kk == 0) return;
+  if (kk == n) {
+    if (rank == 0)
+      for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
+    return;
+  }
+  // this rank's quarter of the row (a multiple of 4 entries: float4 aligned)
+  const int part = ((n + 4 * kTopkRanks - 1) / (4 * kTopkRanks)) * 4;
+  const int q0 = min(n, (int)rank * part), q1 = min(n, q0 + part);
+  float x[8];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {   // entries q0 + 4 (u * kTopkThreads + tid) .. +3
+    const int j = q0 + 4 * (u * kTopkThreads + tid);
+    float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (kVec && j + 3 < q1) {
+      f = *reinterpret_cast<const float4*>(s + j);
+    } else if (j < q1) {
+      f.x = s[j];
+      if (j + 1 < q1) f.y = s[j + 1];
+      if (j + 2 < q1) f.z = s[j + 2];
+      if (j + 3 < q1) f.w = s[j + 3];
+    }
+    x[4 * u] = f.x; x[4 * u + 1] = f.y; x[4 * u + 2] = f.z; x[4 * u + 3] = f.w;
+  }
+  if (rank == 0) {
+    const int words = (n + 31) / 32;
+    for (int i = tid; i < words; i += kTopkThreads) {
+      sm.sel_bits[i] = 0;
+      sm.tie_bits[i] = 0;
+    }
+    if (tid == 0) sm.nC = 0;
+  }
+  for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
+  __syncthreads();
+  int above;
+  const int bstar = find_digit_t<kTopkThreads>(sm.hist, 2048, kk, sm.warp_tot, &above);
+  const int need = kk - above;
+  if ((int)sm.hist[bstar] > kClusterCap) {   // crowded bin (same decision on every rank)
+    if (rank == 0) radix_whole_row<kTopkThreads>(sm, s, n, kk, bstar, need, out, remap, row);
+    return;
+  }
+  const float f_lo = bstar == 0 ? -INFINITY : key_float((uint32_t)bstar << 21);
+  const float f_hi = bstar == 2047 ? __uint_as_float(0x7FFFFFFFu) : key_float((uint32_t)(bstar + 1) << 21);
+  cl_sync();   // rank 0's bitmaps and counter are cleared
+  const uint32_t r_sel = cl_map(sm.sel_bits, 0), r_nc = cl_map(&sm.nC, 0);
+  const uint32_t r_key = cl_map(sm.ckey, 0), r_idx = cl_map(sm.cidx, 0);
+  uint32_t cm = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int j = q0 + 4 * ((u >> 2) * kTopkThreads + tid) + (u & 3);
+    if (j < q1) {
+      if (x[u] >= f_hi) cl_red_or(r_sel + 4u * (uint32_t)(j >> 5), 1u << (j & 31));
+      else if (x[u] >= f_lo) cm |= 1u << u;
+    }
+  }
+  const int c = __popc(cm);
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  const int wtot = __shfl_sync(0xffffffffu, incl, 31);
+  if (wtot) {
+    int base = 0;
+    if (lane == 31) base = (int)cl_atom_add(r_nc, (uint32_t)wtot);
+    base = __shfl_sync(0xffffffffu, base, 31);
+    int pos = base + incl - c;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if ((cm >> u) & 1u) {
+        if (pos < kClusterCap) {
+          cl_st(r_key + 4u * (uint32_t)pos, order_key(x[u]));
+          cl_st(r_idx + 4u * (uint32_t)pos, (uint32_t)(q0 + 4 * ((u >> 2) * kTopkThreads + tid) + (u & 3)));
+        }
+        ++pos;
+      }
+    }
+  }
+  cl_sync();   // every rank's bits and candidates are in rank 0
+  if (rank != 0) return;
+  finish_from_candidates<kTopkThreads, TopkClusterSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kClusterCap), out,
+                                                               remap, row);
+}
+
 // ---- many short rows (prefill: one row per query token) ------------------------------
 // Rows of at most 32,768 entries, many more rows than SMs: a 256-thread CTA
 // per row, six rows per SM, and few instructions per entry.  A sample of the
@@ -1070,6 +1223,29 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     if (e != cudaSuccess) return e;
     return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
                        out_idx, out_cnt, remap);
+  }
+  if (hist && rows * kTopkRanks <= sms && span <= kClusterMaxN && span > kTopkThreads * 8) {
+    // a cluster per row (few rows with a histogram: decode)
+    const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
+    const size_t csm = sizeof(TopkClusterSmem);
+    auto kern = vec ? k_topk_cluster<true> : k_topk_cluster<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * kTopkRanks));
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = csm;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = kTopkRanks;
+    at[1].val.clusterDim.y = 1;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    return counted(cudaLaunchKernelEx(&cfg, kern, scores, stride, v, k, out_idx, out_cnt, remap, hist, hist_stride));
   }
   if (rows <= sms && (hist ? span <= kBitmapMax : span <= (int64_t)kTopkThreads * kHistBatch)) {
     const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;

@@ -183,6 +183,28 @@ def test_topk_bit_exact_rows_in_registers(stride, k):
         assert np.all(idx[r, cnt[r]:] == -1)
 
 
+@pytest.mark.parametrize("stride", [20000, 20001, 32768])
+@pytest.mark.parametrize("k", [512, 2048])
+def test_topk_bit_exact_with_histogram(stride, k):
+    """Row histograms given (the workspace path builds them first): rows of
+    8,193..32,768 entries are spread over a cluster of CTAs per row."""
+    s, nv = _score_rows()
+    s = s[:, :stride].contiguous() if stride <= s.shape[1] else torch.nn.functional.pad(
+        s, (0, stride - s.shape[1]), value=float("nan")).contiguous()
+    nv = torch.clamp(nv, max=stride)
+    rows = s.shape[0]
+    idx = torch.full((rows, k), -5, dtype=torch.int32, device="cuda")
+    cnt = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
+    ws = torch.empty(abi.csa2_topk_workspace_size(rows, stride, k), dtype=torch.uint8, device="cuda")
+    abi.csa2_topk_f32(s.cuda(), nv.cuda(), k, idx, cnt, ws=ws)
+    idx, cnt = idx.cpu().numpy(), cnt.cpu().numpy()
+    for r in range(rows):
+        ref = I.topk(s[r, :nv[r]].numpy(), k)
+        assert cnt[r] == len(ref), r
+        assert np.array_equal(idx[r, :cnt[r]], ref), r
+        assert np.all(idx[r, cnt[r]:] == -1)
+
+
 def _many_short_rows(stride):
     """320 rows (more than twice the SM count) of at most 32,768 entries: the
     four-rows-per-SM path (sampled lower bound, candidates only; the whole-row
