@@ -558,7 +558,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "hierarchical", "ragged"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "hierarchical", "ragged", "encoder_stack", "decoder_stack",
+                             "decoder_stack_prefill"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -106,9 +106,12 @@ __global__ void k_pack_fp8_window(const float* __restrict__ x, int B, int Tq, in
 // RoPE angles: position p = 4e + 3 reaches 4M, so the angle p * theta_i can
 // be ~4e6 rad.  The rotation of frequency i is kept as turns per position,
 // g_i = frac(theta_i / 2 pi) in 0.64 fixed point (host, fp64); p * g_i mod
-// 2^64 in integer arithmetic is then the angle's exact fraction of a turn
-// (error <= p * 2^-53 turns), and sincospi of that fraction in [-1, 1) gives
-// sin and cos.  (fp64 is slow on this GPU; fp32 alone would lose the angle.)
+// 2^64 in integer arithmetic is then the angle's fraction of a turn (error
+// <= p * 2^-53 turns, like the fp64 product p * theta_i), and fp64 sincospi
+// of that fraction and an fp64 rotation give the rotated channels rounded
+// once to fp32, as an fp64 RoPE does: an fp32 rotation moves values across
+// the MXFP4 rounding boundaries now and then.  fp64 is slow on this GPU, so
+// the pairs are spread over the lanes: one angle and one pair per lane.
 constexpr int kNrpWarps = 4;
 struct RopeTurns {
   uint64_t g[256];   // r/2 <= 256 frequencies
@@ -162,28 +165,29 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
     }
   }
   __syncwarp();
-  // rotate-half RoPE on channels [d - r, d) at position 4e + 3
+  // rotate-half RoPE on channels [d - r, d) at position 4e + 3, in fp64: lane
+  // l rotates pair (d - r + l, d - r/2 + l) of each round of 32 pairs in the
+  // row buffer, then the channels' owners read them back
   const int half = r / 2;
   const uint64_t pos = 4ull * (uint64_t)e + 3ull;
+  for (int k0 = 0; k0 < half; k0 += 32) {
+    const int pi = k0 + lane;
+    if (pi < half) {
+      double sn, cs;
+      const uint64_t turns = pos * rope.g[pi];                    // fraction of a turn, mod 2^64
+      sincospi((double)(int64_t)turns * 0x1p-63, &sn, &cs);       // angle / pi in [-1, 1)
+      float* x = row_buf[warp];
+      const double x1 = (double)x[d - r + pi], x2 = (double)x[d - half + pi];
+      x[d - r + pi] = (float)(x1 * cs - x2 * sn);
+      x[d - half + pi] = (float)(x1 * sn + x2 * cs);
+    }
+  }
+  __syncwarp();
   if (has && r > 0) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
       const int ch = lane * 16 + c;
-      if (ch < d - r) continue;
-      const bool first = ch < d - half;
-      const int pi = first ? ch - (d - r) : ch - (d - half);
-      const uint64_t turns = pos * rope.g[pi];                 // fraction of a turn, mod 2^64
-      const float t = (float)(int64_t)turns * 0x1p-63f;        // angle / pi in [-1, 1)
-      float sn, cs;
-      sincospif(t, &sn, &cs);
-      const float self = row_buf[warp][ch];
-      if (first) {
-        const float other = row_buf[warp][ch + half];
-        v[c] = self * cs - other * sn;
-      } else {
-        const float other = row_buf[warp][ch - half];
-        v[c] = other * sn + self * cs;
-      }
+      if (ch >= d - r) v[c] = row_buf[warp][ch];
     }
   }
   if (has) {

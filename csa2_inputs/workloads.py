@@ -250,10 +250,45 @@ def ragged_serving(B: int = 64, lo: int = 8192, hi: int = 1048576, n_short: int 
                                 f"plus {n_short} short ones log-uniform 64..8188, layers F + 5 R")
 
 
+# ---- the pages' 40-layer mode schedule ("DeepSeek-V4.1 架构解析" §02) -------------------
+# 18 encoder layers in three groups of six (one Full, five Reuse); 20 decoder
+# layers in five groups (one Full + three Reuse, then four times one Reindex +
+# three Reuse), the pool built by the decoder's Full layer.
+
+ENCODER_LAYERS = (["F"] + ["R"] * 5) * 3
+DECODER_LAYERS = ["F", "R", "R", "R"] + ["X", "R", "R", "R"] * 4
+
+
+def encoder_stack(B: int = 32, L: int = 131072) -> Workload:
+    """The 18 encoder layers' schedule on the decode shapes (one shared cache)."""
+    return Workload(name=f"encoder_stack_{L // 1024}k_b{B}", seed=5, B=B, t_first=[L] * B, n_new=1,
+                    layers=list(ENCODER_LAYERS),
+                    description=f"{B} sequences x 1 token at {L}, 18 layers 3 x (F + 5 R)")
+
+
+def decoder_stack(B: int = 32, L: int = 131072) -> Workload:
+    """The 20 decoder layers' schedule on the decode shapes, pool from the Full layer."""
+    return Workload(name=f"decoder_stack_{L // 1024}k_b{B}", seed=6, B=B, t_first=[L] * B, n_new=1,
+                    layers=list(DECODER_LAYERS), hierarchical=True,
+                    description=f"{B} sequences x 1 token at {L}, 20 layers (F + 3 R) + 4 x (X + 3 R), "
+                                "pool 2048 blocks x 8")
+
+
+def decoder_stack_prefill(n_new: int = 4096, ctx: int = 65536, H: int = 4096) -> Workload:
+    """The decoder schedule on a prefill chunk: every query token's own pool, Reindex over it."""
+    return Workload(name=f"decoder_stack_prefill_{ctx // 1024}k_chunk{n_new}", seed=7, B=1,
+                    t_first=[ctx - n_new], n_new=n_new, H=H, layers=list(DECODER_LAYERS), hierarchical=True,
+                    description=f"1 sequence, {n_new} new tokens at {ctx - n_new}..{ctx - 1}, hidden {H}, "
+                                "20 layers (F + 3 R) + 4 x (X + 3 R), per-token pools")
+
+
 ALL = {
     "tiny": tiny,
     "decode": decode_128k,
     "prefill": prefill_64k,
     "hierarchical": hierarchical_1m,
     "ragged": ragged_serving,
+    "encoder_stack": encoder_stack,
+    "decoder_stack": decoder_stack,
+    "decoder_stack_prefill": decoder_stack_prefill,
 }

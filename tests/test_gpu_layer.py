@@ -139,6 +139,27 @@ def test_prefill_batch2_with_compression():
         assert np.allclose(kk, new["idx_k"], rtol=2e-2, atol=2e-2)
 
 
+def test_encoder_stack_small():
+    """The pages' encoder schedule, 3 x (F + 5 R): three Full layers re-score
+    the shared cache with their own queries; Reuse layers keep the indices."""
+    wl = WL.encoder_stack(B=2, L=4 * 12000 + 1)
+    check_group(wl, [(0, 0), (1, 0)])
+
+
+def test_decoder_stack_small():
+    """The pages' decoder schedule, (F + 3 R) + 4 x (X + 3 R), with the pool
+    built by the Full layer and searched by every Reindex layer."""
+    wl = WL.decoder_stack(B=2, L=4 * 20000 + 2)
+    check_group(wl, [(0, 0), (1, 0)])
+
+
+def test_decoder_stack_prefill_small():
+    """The decoder schedule on a prefill chunk: each query token's own pool
+    (block maxima from the indexer GEMM), Reindex over the per-token pools."""
+    wl = WL.decoder_stack_prefill(n_new=96, ctx=4096 + 96, H=256)
+    check_group(wl, [(0, 0), (0, 33), (0, 95)])
+
+
 def test_hierarchical_group_small():
     wl = WL.hierarchical_1m(B=2, L=4 * 20000 + 2)
     check_group(wl, [(0, 0), (1, 0)])
