@@ -75,6 +75,9 @@ SIGNATURES = {
     "csa2_compress_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "csa2_compress_pack": (C.c_int, [_P, _I32, _I32, _I32, _P, _P, _F, _F, _P, _P, C.POINTER(Dims),
                                      C.POINTER(Cache), _P, _SZ, _P]),
+    "csa2_compress_layers_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
+    "csa2_compress_layers": (C.c_int, [_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _F, _F, _P, C.POINTER(Dims),
+                                       C.POINTER(Cache), _P, _SZ, _P]),
     "csa2_index_scores": (C.c_int, [C.POINTER(Dims), C.POINTER(Cache), _P, _P, _P, _P, _I64, _P, _I64, _P]),
     "csa2_topk_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "csa2_topk_f32": (C.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
@@ -185,6 +188,22 @@ def csa2_compress_pack(hidden, W, gamma, eps, rope_base, W_idx, first_entry, dim
                                     ptr(first_entry), C.byref(dims), C.byref(cache), ptr(ws),
                                     ws.numel() * ws.element_size() if ws is not None else 0,
                                     stream_handle(stream)))
+
+
+def csa2_compress_layers_workspace_size(B, T, H, L, d, Di) -> int:
+    return lib().csa2_compress_layers_workspace_size(B, T, H, L, d, Di)
+
+
+def csa2_compress_layers(hidden, W_all, Di, gamma_all, eps, rope_base, first_entry, dims: Dims, caches, ws,
+                         stream=None):
+    """caches: a sequence of Cache (one per layer); W_all [L][d + Di][4H]; gamma_all [L][d]."""
+    B, T, H = hidden.shape
+    L = W_all.shape[0]
+    arr = (Cache * L)(*caches)
+    _check(lib().csa2_compress_layers(ptr(hidden), B, T, H, L, ptr(W_all), Di, ptr(gamma_all), eps, rope_base,
+                                      ptr(first_entry), C.byref(dims), arr, ptr(ws),
+                                      ws.numel() * ws.element_size() if ws is not None else 0,
+                                      stream_handle(stream)))
 
 
 def csa2_index_scores(dims: Dims, cache: Cache, idx_q, w, q_pos, scores, blockmax=None, stream=None):

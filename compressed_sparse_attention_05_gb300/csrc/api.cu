@@ -243,6 +243,18 @@ size_t csa2_compress_workspace_size(int32_t B, int32_t T, int32_t H, int32_t d, 
   return compress_partials_bytes(B, T, H, d, Di > 0 ? Di : 0, nullptr);
 }
 
+// The layers' outputs are one GEMM of N = L (d + Di) channels when every layer's block
+// starts on a 128-channel tile (the TMA-fed GEMM); otherwise one call per layer.
+static bool layers_grouped(int32_t H, int32_t d, int32_t Di) {
+  return d % 128 == 0 && (d + Di) % 128 == 0 && H % 16 == 0;
+}
+
+size_t csa2_compress_layers_workspace_size(int32_t B, int32_t T, int32_t H, int32_t L, int32_t d, int32_t Di) {
+  if (B <= 0 || T < 4 || H <= 0 || d <= 0 || L <= 0) return 0;
+  if (!layers_grouped(H, d, Di)) return compress_partials_bytes(B, T, H, d, Di > 0 ? Di : 0, nullptr);
+  return compress_partials_bytes(B, T, H, L * (d + Di), 0, nullptr);
+}
+
 int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, const uint16_t* W,
                        const float* gamma, float eps, float rope_base, const uint16_t* W_idx,
                        const int32_t* first_entry, const csa2_dims* dm, const csa2_cache* c, void* ws,
@@ -278,6 +290,64 @@ int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, 
                                c->page_table, dm->max_pages, c->n_pages, c->kv_codes, c->kv_scales,
                                W_idx ? part + dm->d : nullptr, N, Di, dm->idx_dtype, W_idx ? c->idx_k : nullptr, s),
          "compress_epilogue");
+  return CSA2_OK;
+}
+
+int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, int32_t L,
+                         const uint16_t* W_all, int32_t Di, const float* gamma_all, float eps, float rope_base,
+                         const int32_t* first_entry, const csa2_dims* dm, const csa2_cache* caches, void* ws,
+                         size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc = check_dims(dm, false, false);
+  if (rc) return rc;
+  if (dm->d != 64 && dm->d != 512) return fail(CSA2_ERR_UNSUPPORTED, "d must be 64 or 512 (got %d)", dm->d);
+  REQUIRE(L >= 1 && L <= 4096, "L must be in 1..4096 (got %d)", L);
+  REQUIRE(B == dm->B, "B (%d) must equal dims.B (%d)", B, dm->B);
+  REQUIRE(T >= 0 && H > 0, "T must be >= 0 and H > 0");
+  REQUIRE(H % 64 == 0, "H must be a multiple of 64 (got %d)", H);
+  REQUIRE(Di == 0 || Di == dm->Di, "Di must be 0 or dims.Di (got %d)", Di);
+  REQUIRE(dm->r >= 0 && dm->r <= dm->d && dm->r % 2 == 0, "r must be even and in 0..d");
+  if (B == 0 || T < 4) return CSA2_OK;
+  REQUIRE_PTR(hidden); REQUIRE_PTR(W_all); REQUIRE_PTR(gamma_all); REQUIRE_IPTR(first_entry);
+  REQUIRE(caches, "caches must not be NULL");
+  if (Di) {
+    REQUIRE(Di == 32 || Di == 64 || Di == 128, "Di must be 32, 64 or 128");
+    REQUIRE(dm->idx_dtype == CSA2_BF16 || dm->idx_dtype == CSA2_F32, "bad idx_dtype");
+  }
+  for (int l = 0; l < L; ++l) {
+    rc = check_cache(&caches[l], true, Di > 0);
+    if (rc) return rc;
+  }
+  const int d = dm->d, G = T / 4, Nl = d + Di;
+  const int64_t wl_elems = (int64_t)Nl * 4 * H;   // one layer's stacked weights
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t need = csa2_compress_layers_workspace_size(B, T, H, L, d, Di);
+  if (!ws || ws_bytes < need) return fail(CSA2_ERR_WORKSPACE, "compress_layers needs %zu workspace bytes (got %zu)", need, ws_bytes);
+  REQUIRE(aligned16(ws), "ws must be 16-byte aligned");
+  if (!layers_grouped(H, d, Di)) {   // one compression per layer
+    for (int l = 0; l < L; ++l) {
+      rc = csa2_compress_pack(hidden, B, T, H, W_all + l * wl_elems, gamma_all + (int64_t)l * d, eps, rope_base,
+                              Di ? W_all + l * wl_elems + (int64_t)d * 4 * H : nullptr, first_entry, dm, &caches[l],
+                              ws, ws_bytes, stream);
+      if (rc) return rc;
+    }
+    return CSA2_OK;
+  }
+  // one GEMM: the stacked weights are one [L (d + Di)][4H] operand
+  const int N = L * Nl;
+  int n_split = 1;
+  compress_partials_bytes(B, T, H, N, 0, &n_split);
+  float* part = static_cast<float*>(ws);
+  LAUNCH(launch_compress_gemm(hidden, B, T, H, W_all, N, nullptr, 0, part, n_split, s), "compress_layers_gemm");
+  for (int l = 0; l < L; ++l) {
+    const csa2_cache* c = &caches[l];
+    LatentSource src{part + (int64_t)l * Nl, N, (int64_t)B * G * N, n_split};
+    LAUNCH(launch_norm_rope_pack(src, B, G, d, dm->r, gamma_all + (int64_t)l * d, eps, rope_base, first_entry,
+                                 nullptr, c->page_table, dm->max_pages, c->n_pages, c->kv_codes, c->kv_scales,
+                                 Di ? part + (int64_t)l * Nl + d : nullptr, N, Di, dm->idx_dtype,
+                                 Di ? c->idx_k : nullptr, s),
+           "compress_layers_epilogue");
+  }
   return CSA2_OK;
 }
 

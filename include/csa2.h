@@ -209,6 +209,25 @@ int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H,
                        const csa2_dims* dims, const csa2_cache* cache,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* ---- a1-a4 for several layers from one hidden state --------------------------
+ * "DeepSeek-V4.1 架构解析" §01 (causal encoder-decoder): every decoder layer
+ * projects its KV from the same hidden state (the last encoder layer's) with
+ * its own compression weights.  One GEMM over the layers' stacked weights,
+ * then each layer's RMSNorm, RoPE, MXFP4 pack and paged store (R1-R4, R12)
+ * into its own cache.
+ * hidden bf16 [B][T][H] as for csa2_compress_pack; W_all bf16 [L][d + Di][4H]
+ * (layer l: rows 0..d-1 its W, rows d..d+Di-1 its W_idx); Di = 0 (no indexer
+ * keys written) or dims->Di; gamma_all fp32 [L][d]; caches: host array of L
+ * caches sharing dims (page tables, entry counts and pools may differ).
+ * Entries first_entry[b] .. first_entry[b] + T/4 - 1 of every layer's cache
+ * are written.  Needs csa2_compress_layers_workspace_size() bytes of workspace.
+ * H: multiple of 64; d in {64, 512}; L >= 1. */
+size_t csa2_compress_layers_workspace_size(int32_t B, int32_t T, int32_t H, int32_t L, int32_t d, int32_t Di);
+int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, int32_t L,
+                         const uint16_t* W_all, int32_t Di, const float* gamma_all, float eps,
+                         float rope_base, const int32_t* first_entry, const csa2_dims* dims,
+                         const csa2_cache* caches, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- a5: index scores of every visible entry (R6, R7) ----------------------
  * idx_q [B][Tq][Hi][Di] (idx_dtype), w fp32 [B][Tq][Hi], q_pos int32 [B][Tq].
  * scores fp32 [B*Tq][score_stride]: column j < n_vis(row) receives s_j;

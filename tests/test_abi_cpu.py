@@ -116,3 +116,21 @@ def test_compress_validation(lib):
     rc = lib.csa2_compress_pack(FAKE, 2, 64, 128, FAKE, FAKE, 1e-6, 1e4, FAKE, FAKE, C.byref(dm), C.byref(c),
                                 FAKE, need - 1, None)
     assert rc == 4
+
+
+def test_compress_layers_validation(lib):
+    dm, c = _dims(), _cache()
+    caches = (abi.Cache * 2)(c, c)
+    rc = lib.csa2_compress_layers(FAKE, 2, 64, 128, 0, FAKE, 128, FAKE, 1e-6, 1e4, FAKE, C.byref(dm), caches,
+                                  FAKE, 1 << 30, None)
+    assert rc == 1 and "L must be" in lib_err()
+    rc = lib.csa2_compress_layers(FAKE, 2, 64, 128, 2, FAKE, 96, FAKE, 1e-6, 1e4, FAKE, C.byref(dm), caches,
+                                  FAKE, 1 << 30, None)
+    assert rc == 1 and "Di must be" in lib_err()
+    # grouped: one workspace for all layers' outputs, larger than one layer's
+    one = abi.csa2_compress_workspace_size(2, 64, 128, 512, 128)
+    assert abi.csa2_compress_layers_workspace_size(2, 64, 128, 2, 512, 128) > one
+    need = abi.csa2_compress_layers_workspace_size(2, 64, 128, 2, 512, dm.Di)
+    rc = lib.csa2_compress_layers(FAKE, 2, 64, 128, 2, FAKE, dm.Di, FAKE, 1e-6, 1e4, FAKE, C.byref(dm), caches,
+                                  FAKE, need - 1, None)
+    assert rc == 4
