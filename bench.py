@@ -268,6 +268,159 @@ def run_gpu(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------------
+# the decoder layers' KV from one hidden state (csa2_compress_layers)
+
+CED_LAYERS = 20   # the decoder layers of the pages' 40-layer model
+
+
+def ced_setup(dev):
+    """The prefill chunk's hidden states and CED_LAYERS layers' stacked weights, one
+    page pool per layer (the chunk's 1,024 entries after 15,360 cached ones)."""
+    import torch
+
+    from compressed_sparse_attention_05_gb300 import abi
+    wl = make_workload("prefill")
+    G = wl.n_new // 4
+    first = wl.entries_before(0)
+    pages = (first + G + 63) // 64
+    hidden = wl.hidden(dev)
+    W_all = wl.w_layers(CED_LAYERS, dev)
+    gamma = torch.stack([wl.gamma(dev)] * CED_LAYERS)
+    keep, caches = [], []
+    for l in range(CED_LAYERS):
+        t = {"codes": torch.zeros(pages * 64, wl.d // 2, dtype=torch.uint8, device=dev),
+             "scales": torch.zeros(pages * 64, wl.d // 16, dtype=torch.uint8, device=dev),
+             "idx": torch.zeros(pages * 64, wl.Di, dtype=torch.bfloat16, device=dev),
+             "pt": torch.arange(pages, dtype=torch.int32, device=dev).reshape(1, pages),
+             "n": torch.tensor([first + G], dtype=torch.int32, device=dev)}
+        keep.append(t)
+        caches.append(abi.Cache(kv_codes=t["codes"].data_ptr(), kv_scales=t["scales"].data_ptr(),
+                                idx_k=t["idx"].data_ptr(), page_table=t["pt"].data_ptr(),
+                                n_entries=t["n"].data_ptr(), n_pages=pages))
+    dims = abi.Dims(B=1, Tq=wl.n_new, d=wl.d, r=wl.r, Hq=wl.Hq, Hi=wl.Hi, Di=wl.Di, idx_dtype=abi.CSA2_BF16,
+                    K=wl.K, W=wl.W, max_pages=pages, n_pool_blocks=0, pool_block=8, swa_cap=0)
+    fe = torch.tensor([first], dtype=torch.int32, device=dev)
+    ws = torch.empty(abi.csa2_compress_layers_workspace_size(1, wl.n_new, wl.H, CED_LAYERS, wl.d, wl.Di),
+                     dtype=torch.uint8, device=dev)
+
+    def step():
+        abi.csa2_compress_layers(hidden, W_all, wl.Di, gamma, wl.eps, wl.rope_base, fe, dims, caches, ws)
+
+    return wl, hidden, keep, step
+
+
+def run_ced(args, rank, world, dist):
+    """--workload ced_compress: one step = CED_LAYERS layers' KV of the prefill chunk
+    from one hidden state (one GEMM over the stacked weights, per-layer pack)."""
+    import torch
+
+    from compressed_sparse_attention_05_gb300 import abi, build
+
+    build.build()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl, hidden, keep, step = ced_setup(dev)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    for w in range(args.warmup):
+        flush(w)
+        step()
+    torch.cuda.synchronize()
+    assert abi.csa2_get_status() == 0
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    n0 = abi.csa2_launch_count()
+    with ClockSampler(local) as clk:
+        for k in range(args.steps):
+            flush(k)
+            ev[k][0].record(stream)
+            step()
+            ev[k][1].record(stream)
+        torch.cuda.synchronize()
+    launches = abi.csa2_launch_count() - n0
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(step_ms) / args.steps, dist, dev)
+    # end to end: the chunk's hidden states in from pinned host memory, the last layer's codes back
+    h_in = hidden.cpu().pin_memory()
+    h_out = torch.empty(keep[-1]["codes"].shape, dtype=torch.uint8, pin_memory=True)
+    n = max(3, min(args.steps, 50))
+    tot = 0.0
+    for k in range(n):
+        flush(k)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        hidden.copy_(h_in, non_blocking=True)
+        step()
+        h_out.copy_(keep[-1]["codes"], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    e2e_ms = max_over_ranks(tot / n, dist, dev)
+    status = abi.csa2_get_status()
+    if rank != 0:
+        return
+    G = wl.n_new // 4
+    flops = 2.0 * G * 4 * wl.H * CED_LAYERS * (wl.d + wl.Di)
+    peaks = load_peaks()
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": world * wl.n_new / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"ced_compress_{CED_LAYERS}layers_chunk{wl.n_new}",
+                   "description": f"{CED_LAYERS} layers' KV of a {wl.n_new}-token chunk (hidden {wl.H}) from one "
+                                  "hidden state: one GEMM over the stacked weights, per-layer RMSNorm/RoPE/MXFP4",
+                   "tokens_per_step": wl.n_new, "layers": CED_LAYERS, "d": wl.d, "Di": wl.Di,
+                   "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "k_compress_gemm_tma (+ k_norm_rope_pack per layer)",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None, "algorithmic_flops_per_launch": flops,
+                     "kernel_ms": ms, "peak_source": peaks["source"] + " (bf16 burst)"},
+        "e2e": {"value": world * wl.n_new / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": hidden.numel() * 2, "d2h_bytes_per_step": h_out.numel()},
+        "gpu_launches": launches, "status_word": status,
+        "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms), "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline("ced_compress", args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def ced_cpu_worker(seconds, ref_steps=0):
+    """The oracle's compression of the chunk for one layer (whole layers until `seconds`
+    are used, at least one), scaled to CED_LAYERS layers."""
+    import torch
+    torch.set_num_threads(1)
+    from oracle import compress as Cm
+    wl = make_workload("prefill")
+    hid = wl.hidden()[0].double().numpy()
+    W_all = wl.w_layers(1)
+    gamma = wl.gamma().double().numpy()
+    first = wl.entries_before(0)
+    W, Wi = W_all[0, :wl.d].double().numpy(), W_all[0, wl.d:].double().numpy()
+    times = []
+    t_tot = 0.0
+    while not times or t_tot < seconds:
+        t0 = time.perf_counter()
+        Cm.compress_pack(hid, W, gamma, wl.eps, wl.r, wl.rope_base, first, W_idx=Wi)
+        times.append(time.perf_counter() - t0)
+        t_tot += times[-1]
+    per_layer = t_tot / len(times)
+    value = wl.n_new / (per_layer * CED_LAYERS)
+    out = {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+           "sample": f"{len(times)} layer(s) of the {wl.n_new}-token chunk's compression, {t_tot:.1f} s of "
+                     f"single-thread float64 numpy, scaled to {CED_LAYERS} layers"}
+    if ref_steps > 0:
+        out["step_values"] = [wl.n_new / (t * CED_LAYERS) for t in times] * ref_steps
+        out["step_values"] = out["step_values"][:ref_steps]
+    print(json.dumps(out))
+
+
 class L2Flush:
     """Evicts the step's inputs from L2: writes FLUSH_BYTES, then reads another
     FLUSH_BYTES, so that the L2 ends up holding clean lines of neither."""
@@ -545,12 +698,14 @@ def run_reference(args, rank, world):
     # aggregate over the timed steps: total tokens / total seconds (harmonic mean of the step rates)
     value = len(timed) / sum(1.0 / v for v in timed) if timed else r["value"]
     last = r
-    wl = make_workload(args.workload)
+    wl = make_workload("prefill" if args.workload == "ced_compress" else args.workload)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": wl.B * wl.Tq / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description},
+        "config": ({"workload": f"ced_compress_{CED_LAYERS}layers_chunk{wl.n_new}",
+                    "description": f"{CED_LAYERS} layers' KV of a {wl.n_new}-token chunk from one hidden state"}
+                   if args.workload == "ced_compress" else {"workload": wl.name, "description": wl.description}),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -564,7 +719,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "hierarchical", "ragged", "encoder_stack", "decoder_stack",
-                             "decoder_stack_prefill"])
+                             "decoder_stack_prefill", "ced_compress"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,
@@ -574,7 +729,10 @@ def main():
     ap.add_argument("--cpu-worker", action="store_true")
     args = ap.parse_args()
     if args.cpu_worker:
-        cpu_worker(args.workload, args.cpu_seconds, args.ref_steps)
+        if args.workload == "ced_compress":
+            ced_cpu_worker(args.cpu_seconds, args.ref_steps)
+        else:
+            cpu_worker(args.workload, args.cpu_seconds, args.ref_steps)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -590,6 +748,8 @@ def main():
         dist = dist_mod
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload == "ced_compress":
+        run_ced(args, rank, world, dist)
     else:
         run_gpu(args, rank, world, dist)
     if dist is not None:

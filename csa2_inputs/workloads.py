@@ -181,6 +181,15 @@ class Workload:
         """bf16 [Di, 4H]: projection of the concatenated group onto the indexer key."""
         return (rng.normal(self._key("w_i"), (self.Di, 4 * self.H), device) * 0.02).to(torch.bfloat16)
 
+    def w_layers(self, n_layers: int, device="cpu") -> torch.Tensor:
+        """bf16 [n_layers][d + Di][4H]: each layer's own compression map and indexer-key
+        projection, stacked (the decoder layers' KV from one hidden state)."""
+        out = torch.empty(n_layers, self.d + self.Di, 4 * self.H, dtype=torch.bfloat16, device=device)
+        for l in range(n_layers):
+            out[l] = (rng.normal(self._key("w_layer", l), (self.d + self.Di, 4 * self.H), device) * 0.02).to(
+                torch.bfloat16)
+        return out
+
     def gamma(self, device="cpu") -> torch.Tensor:
         return 1.0 + 0.05 * rng.normal(self._key("gamma"), (self.d,), device)
 
