@@ -146,17 +146,18 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
 }
 
 // ---- tcgen05 + TMA path -------------------------------------------------------------
-// CTA tile 128 entries x 128 output channels; K in 64-wide stages of 32 KB
-// (A then B, both 128-byte-swizzled K-major) in a 6-stage ring filled by
+// CTA tile 128 entries x 256 output channels; K in 64-wide stages of 48 KB
+// (A then B, both 128-byte-swizzled K-major) in a 4-stage ring filled by
 // tensor-map copies: A is the hidden states seen as [B][G][4H] (row j of
-// batch b starts at token 4j), B is W or W_idx.  Warp 0 issues the copies,
-// warp 1 the MMAs (M = 128, N = 128, K = 16) into a 128-column fp32
+// batch b starts at token 4j), B is W or W_idx (W_idx tiles hold Di rows;
+// the tile's other columns are never stored).  Warp 0 issues the copies,
+// warp 1 the MMAs (M = 128, N = 256, K = 16) into a 256-column fp32
 // accumulator in tensor memory, warps 2..5 write the fp32 partial sums.
 // Split K: grid.z = B x n_split, split s takes stages [s n / n_split,
 // (s + 1) n / n_split).  Every wait is bounded.
-constexpr int kTmM = 128, kTmN = 128, kTmK = 64, kTmStages = 6;
+constexpr int kTmM = 128, kTmN = 256, kTmK = 64, kTmStages = 4;
 constexpr int kTmABytes = kTmM * kTmK * 2;                 // 16 KB
-constexpr int kTmStageBytes = kTmABytes + kTmN * kTmK * 2;   // 32 KB
+constexpr int kTmStageBytes = kTmABytes + kTmN * kTmK * 2;   // 48 KB
 constexpr int kTmEpiWarps = 4;
 constexpr int kTmThreads = (2 + kTmEpiWarps) * 32;
 constexpr int kTmSmsTarget = 152;   // splits fill this many SMs once (the GPU's SM count)
@@ -179,8 +180,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 
 __global__ void __launch_bounds__(kTmThreads, 1)
 k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
-                    const __grid_constant__ CUtensorMap imap, int G, int d, int N, int M, int n_stages, int n_split,
-                    float* __restrict__ partials, uint32_t* status) {
+                    const __grid_constant__ CUtensorMap imap, int G, int d, int Di, int N, int M, int n_stages,
+                    int n_split, float* __restrict__ partials, uint32_t* status) {
   extern __shared__ unsigned char smem_raw[];
   pdl_trigger();
   pdl_wait();
@@ -215,7 +216,7 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
       for (int i = 0; i < my; ++i) {
         const int st = i % kTmStages;
         if (i >= kTmStages && !wait_or_abort(&sm.empty[st], ((i / kTmStages) - 1) & 1, abort)) break;
-        tc::mbar_arrive_expect_tx(&sm.full[st], kTmStageBytes);
+        tc::mbar_arrive_expect_tx(&sm.full[st], (uint32_t)(kTmABytes + (n0 < d ? kTmN : Di) * kTmK * 2));
         const int kx = (s0 + i) * kTmK;
         tma::load_3d(sm.ring[st], &amap, kx, j0, b, &sm.full[st]);
         if (n0 < d) tma::load_2d(sm.ring[st] + kTmABytes, &wmap, kx, n0, &sm.full[st]);
@@ -274,8 +275,11 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
   if (tid == 0 && *abort) raise_status(status, CSA2_STATUS_TIMEOUT);
 }
 
+// W_idx tiles start on a tile (d a multiple of 256); without W_idx any d >= 256 with
+// 16-byte rows of output works (the last tile's rows past d are zero-filled).
 static bool tma_compress_ok(int T, int H, int d, int Di) {
-  return d % kTmN == 0 && H % 16 == 0 && T >= 4 && Di % 4 == 0 && Di <= kTmN && tensor_map_encoder() != nullptr;
+  return (Di ? d % kTmN == 0 : (d >= kTmN && d % 4 == 0)) && H % 16 == 0 && T >= 4 && Di % 4 == 0 &&
+         Di <= kTmN && tensor_map_encoder() != nullptr;
 }
 
 // Split K only as far as it takes to fill the SMs once.
@@ -308,6 +312,7 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
     const cuuint64_t wstr[1] = {(cuuint64_t)Kd * 2};
     const cuuint32_t wbox[2] = {kTmK, kTmN};
     const cuuint64_t idims[2] = {(cuuint64_t)Kd, (cuuint64_t)(W_idx ? Di : d)};
+    const cuuint32_t ibox[2] = {kTmK, (cuuint32_t)(W_idx ? Di : kTmN)};
     EncodeTiled enc = tensor_map_encoder();
     if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(hidden), adims, astr, abox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -315,7 +320,7 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
         enc(&wmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W), wdims, wstr, wbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-        enc(&imap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W_idx ? W_idx : W), idims, wstr, wbox,
+        enc(&imap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W_idx ? W_idx : W), idims, wstr, ibox,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -323,8 +328,8 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
     cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((N + kTmN - 1) / kTmN, (G + kTmM - 1) / kTmM, B * n_split);
-    return launch_step(k_compress_gemm_tma, grid, dim3(kTmThreads), smem, s, amap, wmap, imap, G, d, N, M,
-                       Kd / kTmK, n_split, partials, status_word());
+    return launch_step(k_compress_gemm_tma, grid, dim3(kTmThreads), smem, s, amap, wmap, imap, G, d,
+                       W_idx ? Di : 0, N, M, Kd / kTmK, n_split, partials, status_word());
   }
   dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
   k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M, partials);
