@@ -396,7 +396,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       sm.slot[c * kChunk + key] =
           key_source(a, row, b, (c0 + c) * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, true, status);
   }
-  // ---- round 4: the first chunk's packed bytes
+  // ---- the first chunk's packed bytes
   float cur_wsc = 0.f;
   uint2 cur_sc = make_uint2(0, 0);
   KeyBytes kb;
