@@ -16,6 +16,8 @@ Value recipe (same for every workload; each tensor has its own stream):
   indexer queries        ~N(0,1), same dtype as the keys; head weights ~N(0,1) fp32
   attention queries Q    ~N(0,1), bf16
   sliding-window latent  ~N(0,1), fp32 (each side packs it to FP8 itself)
+  replayed hidden states ~N(0,1), about 0.1% of elements replaced by +/-10, bf16, one
+                         tensor per layer (window rebuilt by SWA Bounded Replay)
   page table             random permutation of the shared page pool
 """
 from __future__ import annotations
@@ -53,6 +55,7 @@ class Workload:
     pool_block: int = 8
     rope_base: float = 10000.0
     eps: float = 1e-6
+    replay_H: Optional[int] = None  # SWA Bounded Replay: hidden size of the replayed tokens
     description: str = ""
 
     # ---- derived structure -------------------------------------------------
@@ -61,7 +64,12 @@ class Workload:
         return self.n_new
 
     def entries_before(self, b: int) -> int:
-        """Compressed entries already cached before this step (complete groups of 4)."""
+        """Compressed entries already cached before this step (complete groups of 4).
+
+        A replay step re-runs tokens whose compressed entries are already in the
+        persistent cache: the cache then covers every replayed token too."""
+        if self.replay_H is not None:
+            return (self.t_first[b] + self.n_new) // 4
         return self.t_first[b] // 4
 
     def new_entries(self, b: int) -> int:
@@ -101,15 +109,20 @@ class Workload:
         return pt
 
     # sliding-window rows held per sequence: the W-1 tokens before the first
-    # new token (already packed state) plus the new tokens themselves
+    # new token (already packed state) plus the new tokens themselves; a replay
+    # step rebuilds the window from its replayed tokens alone
     def swa_pos0(self) -> torch.Tensor:
+        if self.replay_H is not None:
+            return torch.tensor(self.t_first, dtype=torch.int32)
         return torch.tensor([max(0, t - (self.W - 1)) for t in self.t_first], dtype=torch.int32)
 
     @property
     def swa_cap(self) -> int:
-        return (self.W - 1) + self.n_new
+        return self.n_new if self.replay_H is not None else (self.W - 1) + self.n_new
 
     def swa_rows_before(self, b: int) -> int:
+        if self.replay_H is not None:
+            return 0
         return self.t_first[b] - max(0, self.t_first[b] - (self.W - 1))
 
     # ---- raw tensors ---------------------------------------------------------
@@ -172,6 +185,27 @@ class Workload:
         v = rng.normal_at(self._key("hidden"), idx)
         v = rng.with_outliers(self._key("hidden_outlier"), idx, v, 1000, 10.0)
         return v.to(torch.bfloat16)
+
+    def replay_hidden(self, layer: int, device="cpu") -> torch.Tensor:
+        """bf16 [B, n_new, replay_H]: layer ``layer``'s hidden states of the replayed tokens."""
+        shape = (self.B, self.n_new, self.replay_H)
+        idx = torch.arange(self.B * self.n_new * self.replay_H, dtype=torch.int64, device=device).reshape(shape)
+        return self._replay_values(layer, idx)
+
+    def replay_hidden_rows(self, layer: int, b: int) -> torch.Tensor:
+        """bf16 [n_new, replay_H]: sequence b of replay_hidden(layer), element for element."""
+        n = self.n_new * self.replay_H
+        idx = torch.arange(b * n, (b + 1) * n, dtype=torch.int64).reshape(self.n_new, self.replay_H)
+        return self._replay_values(layer, idx)
+
+    def _replay_values(self, layer: int, idx: torch.Tensor) -> torch.Tensor:
+        v = rng.normal_at(self._key("replay_hidden", layer), idx)
+        v = rng.with_outliers(self._key("replay_outlier", layer), idx, v, 1000, 10.0)
+        return v.to(torch.bfloat16)
+
+    def w_swa(self, layer: int, device="cpu") -> torch.Tensor:
+        """bf16 [d, replay_H]: layer ``layer``'s projection of a token onto its window row."""
+        return (rng.normal(self._key("w_swa", layer), (self.d, self.replay_H), device) * 0.02).to(torch.bfloat16)
 
     def w_compress(self, device="cpu") -> torch.Tensor:
         """bf16 [d, 4H]: the learned 4:1 compression map (row o = output channel o)."""
@@ -291,6 +325,17 @@ def decoder_stack_prefill(n_new: int = 4096, ctx: int = 65536, H: int = 4096) ->
                                 "20 layers (F + 3 R) + 4 x (X + 3 R), per-token pools")
 
 
+def decoder_replay(B: int = 8, L: int = 131072, n_win: int = 128, H: int = 4096) -> Workload:
+    """SWA Bounded Replay ("DeepSeek-V4.1 架构解析" §03) on the decoder: each of the 20
+    decoder layers rebuilds its window from the last n_win tokens of every sequence
+    and runs its step for those tokens, over the persistent compressed cache."""
+    return Workload(name=f"decoder_replay_{L // 1024}k_b{B}_win{n_win}", seed=8, B=B, t_first=[L - n_win] * B,
+                    n_new=n_win, layers=list(DECODER_LAYERS), hierarchical=True, replay_H=H,
+                    description=f"{B} sequences, the last {n_win} of {L} tokens replayed through the 20 decoder "
+                                f"layers (F + 3 R) + 4 x (X + 3 R): per layer window rows from hidden {H}, "
+                                "then the layer step for the replayed tokens, per-token pools")
+
+
 ALL = {
     "tiny": tiny,
     "decode": decode_128k,
@@ -300,4 +345,5 @@ ALL = {
     "encoder_stack": encoder_stack,
     "decoder_stack": decoder_stack,
     "decoder_stack_prefill": decoder_stack_prefill,
+    "decoder_replay": decoder_replay,
 }

@@ -16,6 +16,8 @@ citing the passage it follows:
   indexer    a5 index scores, a6 Top-K, a7 block pool, a8 Reindex, a9 Reuse
   attention  a10/a11 sparse MQA attention over selected entries + window,
              and an independent dense masked form
+  replay     SWA Bounded Replay: window rows rebuilt from the replayed
+             tokens' hidden states, and the window cut at the replay start
   layer      the layer schedule (Full / Reindex / Reuse) for sampled tokens
 
 Pins (tests/test_oracle_*.py, run with ``-m "not gpu"``) tie every function

@@ -15,7 +15,9 @@ in the order the pages give (DeepSeek-V4.1 architecture analysis
   Reuse    take the previous layer's indices unchanged, attend.
 
 Every layer has its own attention query Q and its own sliding window; the
-compressed KV and the indexer keys are shared by the group.
+compressed KV and the indexer keys are shared by the group.  A replay
+workload (SWA Bounded Replay, §03) rebuilds each layer's window from its
+replayed tokens (``replay``) and cuts the window at the first of them.
 
 Inputs come from ``csa2_inputs.workloads`` (raw random tensors); every step
 of arithmetic on them is done here.  The functions only touch the rows they
@@ -26,7 +28,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import attention, compress, formats, indexer
+from . import attention, compress, formats, indexer, replay
 
 
 def _np(x: torch.Tensor) -> np.ndarray:
@@ -43,7 +45,7 @@ class SequenceState:
         self.gamma = _np(wl.gamma())
         self._new = None
         self._idx_k = None
-        self._swa = {}
+        self._replay = {}
 
     # new entries produced by this step's compression (Full layer of a prefill)
     def new_entries(self):
@@ -87,12 +89,34 @@ class SequenceState:
         c, s = self.packed_rows(rows)
         return formats.mxfp4_unpack(c, s)
 
+    def replay_rows(self, layer: int):
+        """Window rows of layer ``layer`` rebuilt from the replayed tokens (SWA Bounded Replay)."""
+        if layer not in self._replay:
+            wl = self.wl
+            self._replay[layer] = replay.window_rows(
+                _np(wl.replay_hidden_rows(layer, self.b)), _np(wl.w_swa(layer)), self.gamma, wl.eps, wl.r,
+                wl.rope_base, wl.t_first[self.b])
+        return self._replay[layer]
+
     def swa_rows(self, layer: int, positions: np.ndarray) -> np.ndarray:
         """Dequantised window rows (bf16 values as float64) of raw tokens ``positions``."""
         positions = np.asarray(positions, dtype=np.int64)
+        if self.wl.replay_H is not None:
+            rows = self.replay_rows(layer)
+            k = positions - self.wl.t_first[self.b]
+            assert np.all((k >= 0) & (k < self.wl.n_new)), "the rebuilt window holds only replayed tokens"
+            return formats.fp8_unpack_bf16(rows["codes"][k], rows["scales"][k])
         lat = _np(self.wl.swa_latent(layer, self.b, torch.from_numpy(positions)))
         codes, scales = formats.fp8_pack(lat)
         return formats.fp8_unpack_bf16(codes, scales)
+
+
+def window_of(wl, b: int, t: int) -> np.ndarray:
+    """Raw positions of the window rows the token at t of sequence b attends to: the
+    last W tokens, cut at the first replayed token when the window was rebuilt."""
+    if wl.replay_H is not None:
+        return replay.replay_window_positions(t, wl.W, wl.t_first[b])
+    return attention.window_positions(t, wl.W)
 
 
 def run_group(wl, samples, layers=None, want_scores=False):
@@ -141,7 +165,7 @@ def run_group(wl, samples, layers=None, want_scores=False):
             prev_idx = idx
             if layer in layers:
                 Q = _np(wl.q_row(layer, b, i))
-                swa_pos = attention.window_positions(t, wl.W)
+                swa_pos = window_of(wl, b, t)
                 O, lse = attention.sparse_attention(Q, st.kv_rows(idx),
                                                     st.swa_rows(layer, swa_pos), tau)
                 res.update(idx=indexer.pad(idx, wl.K), cnt=len(idx), O=O, lse=lse, t=t)

@@ -76,3 +76,17 @@ def test_ragged_lengths_cover_truncation():
     assert sum(x < 2048 for x in n) == 6
     assert any(x < 512 for x in n)     # Top-512 truncates for some sequence
     assert max(n) <= 1048576 // 4
+
+
+def test_replay_workload_layout():
+    # SWA Bounded Replay: the queries are the last n_win tokens, the compressed
+    # cache covers them, and each layer's window holds only the replayed rows
+    wl = workloads.decoder_replay(B=3, L=4 * 3000 + 40, n_win=40, H=128)
+    assert wl.Tq == 40 and wl.swa_cap == 40
+    for b in range(wl.B):
+        assert wl.entries_before(b) == wl.entries_after(b) == (4 * 3000 + 40) // 4
+        assert wl.swa_rows_before(b) == 0
+        assert int(wl.swa_pos0()[b]) == int(wl.q_pos()[b, 0]) == 4 * 3000
+        assert torch.equal(wl.replay_hidden_rows(5, b), wl.replay_hidden(5)[b])
+    assert not torch.equal(wl.replay_hidden(0), wl.replay_hidden(1))   # a stream per layer
+    assert wl.w_swa(0).shape == (wl.d, 128) and not torch.equal(wl.w_swa(0), wl.w_swa(1))

@@ -10,7 +10,8 @@ import test_oracle_attention as TA
 import test_oracle_compress as TC
 import test_oracle_formats as TF
 import test_oracle_indexer as TI
-from oracle import attention, compress, formats, indexer
+import test_oracle_replay as TR
+from oracle import attention, compress, formats, indexer, replay
 
 
 def _concat_feature_major(hidden):
@@ -93,6 +94,25 @@ def _e4m3_ties_away(x):
     return (best | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
 
 
+_good_rows = replay.window_rows
+
+
+def _rows_rotated_at_row_index(hidden, W_swa, gamma, eps, r, base, pos0):
+    return _good_rows(hidden, W_swa, gamma, eps, r, base, 0)
+
+
+def _rows_rotated_at_entry_position(hidden, W_swa, gamma, eps, r, base, pos0):
+    return _good_rows(hidden, W_swa, gamma, eps, r, base, pos0 + 3)
+
+
+def _replay_window_one_too_long(t, W, p0):
+    return np.arange(max(p0, t - W), t + 1, dtype=np.int64)
+
+
+def _replay_window_not_cut(t, W, p0):
+    return np.arange(max(0, t - W + 1), t + 1, dtype=np.int64)
+
+
 CASES = [
     ("compress", "concat_groups", _concat_feature_major, TC.test_selection_map_picks_token_and_channel),
     ("compress", "rmsnorm", _rms_no_gamma, TC.test_rmsnorm_gain_and_scale_invariance),
@@ -107,9 +127,17 @@ CASES = [
     ("attention", "softmax_attention", _attn_no_scale, TA.test_matches_torch_sdpa),
     ("formats", "mxfp4_pack", _pack_swapped_nibbles, TF.test_mxfp4_hand_example),
     ("formats", "e4m3_encode_array", _e4m3_ties_away, TF.test_e4m3_encoder_matches_torch_cast),
+    ("replay", "window_rows", _rows_rotated_at_row_index, TR.test_window_row_is_compression_of_the_groups_last_token),
+    ("replay", "window_rows", _rows_rotated_at_entry_position,
+     TR.test_window_row_is_compression_of_the_groups_last_token),
+    ("replay", "replay_window_positions", _replay_window_one_too_long,
+     TR.test_replay_window_matches_brute_force_and_is_cut_at_the_replay_start),
+    ("replay", "replay_window_positions", _replay_window_not_cut,
+     TR.test_replay_window_matches_brute_force_and_is_cut_at_the_replay_start),
 ]
 
-_MODULES = {"compress": compress, "indexer": indexer, "attention": attention, "formats": formats}
+_MODULES = {"compress": compress, "indexer": indexer, "attention": attention, "formats": formats,
+            "replay": replay}
 
 
 @pytest.mark.parametrize("mod,name,bad,pin", CASES, ids=[f"{m}.{n}-{b.__name__}" for m, n, b, _ in CASES])
