@@ -1,6 +1,7 @@
 """Benchmark of the CSA2 layer step on GB300 (prints one JSON line).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|hierarchical|ragged]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|hierarchical|ragged|
+                    encoder_stack|decoder_stack|decoder_stack_prefill|decoder_replay|ced_compress]
     python bench.py --impl reference ...      # the CPU oracle on a bounded sample
 
 A step is one pass of the layer group over one batch of synthetic input,
@@ -42,7 +43,8 @@ def algorithmic(wl):
 
     Bytes count what a step must move at least once: each sequence's visible
     indexer keys per Full layer (all query tokens of a sequence share them),
-    the pooled keys per Reindex query, the selected MXFP4 entries (at most the
+    the pooled keys per Reindex layer (the pools of one sequence's tokens overlap,
+    so at most its visible keys), the selected MXFP4 entries (at most the
     entries that exist), the queries read, the outputs written and the index
     scores written and read back once, plus the hidden states of a prefill
     chunk.  For one query token per sequence this is the per-query sum.
@@ -63,27 +65,35 @@ def algorithmic(wl):
             if mode == "F":
                 scan += max(nvs) * Di * idx_elt
             sel = 0
+            pooled_seq = 0
             for i in range(wl.Tq):
                 t = wl.t_first[b] + i
                 nv = nvs[i]
                 nk = min(K, nv)
-                nwin = min(W, t + 1)
+                # a rebuilt window (SWA Bounded Replay) starts at the first replayed token
+                nwin = min(W, t + 1) if wl.replay_H is None else min(W, i + 1)
                 sel += nk
                 if mode == "F":
                     idx_flops += 2 * nv * wl.Hi * Di
                     io += 2 * nv * 4                     # score written, read back by the Top-K
                 elif mode == "X":
                     npos = min(nv, wl.pool_blocks * wl.pool_block)
-                    pooled += npos * Di * idx_elt
+                    pooled_seq += npos
                     idx_flops += 2 * npos * wl.Hi * Di
                     io += 2 * npos * 4
                 attn_flops += 4 * Hq * d * (nk + nwin)
             gathered += min(sel, n_ent) * entry_bytes
+            pooled += min(pooled_seq, max(nvs)) * Di * idx_elt   # a sequence's pools overlap: unique keys
             io += wl.Tq * Hq * d * (2 + 4)                # Q (bf16) in, O (fp32) out
     compress_flops = 0
     if wl.H is not None:
         compress_flops = 2 * sum(wl.new_entries(b) for b in range(wl.B)) * 4 * wl.H * (d + Di)
         io += wl.B * wl.Tq * wl.H * 2                     # hidden states (bf16)
+    if wl.replay_H is not None:
+        # every layer projects its replayed tokens onto window rows: hidden states in, FP8 rows out
+        n_rows = wl.B * wl.Tq * len(wl.layers)
+        compress_flops += 2 * n_rows * wl.replay_H * d
+        io += n_rows * (wl.replay_H * 2 + d + 4)
     n_full = max(1, sum(1 for m in wl.layers if m == "F"))
     return {"scan_bytes": scan, "pooled_bytes": pooled, "gathered_bytes": gathered, "io_bytes": io,
             "step_bytes": scan + pooled + gathered + io, "attn_flops": attn_flops, "index_flops": idx_flops,
@@ -444,12 +454,12 @@ def time_dominant_kernel(args, g, wl, flush, stream):
     from compressed_sparse_attention_05_gb300 import abi
 
     n = max(3, min(args.steps, 200))
-    if wl.H is None:   # decode-type workloads: the Full layer's indexer scan
+    if wl.Tq == 1:     # decode-type workloads: the Full layer's indexer scan
         stride = g.max_entries
         scores = torch.empty(wl.B * wl.Tq, stride, dtype=torch.float32, device=flush.device)
         fn = lambda: abi.csa2_index_scores(g.dims(), g.cache(), g.idx_q[0], g.idx_w[0], g.q_pos, scores)  # noqa
         name = "k_index_scan_pages"
-    else:              # prefill: attention of the Full layer
+    else:              # prefill and replay: attention of the Full layer
         fn = lambda: abi.csa2_sparse_attn(g.dims(), g.cache(), g.window(0), g.Q[0], g.q_pos, g.idx[0],  # noqa
                                           g.cnt[0], 1.0 / math.sqrt(wl.d), g.O[0], g.lse[0])
         name = "k_sparse_attn_tc"
@@ -569,9 +579,12 @@ def cpu_worker(workload, seconds, ref_steps=0):
     from oracle import formats as F
     from oracle import indexer as I
     from oracle import layer as OL
+    from oracle import replay as R
 
     wl = make_workload(workload)
     tau = 1.0 / math.sqrt(wl.d)
+    replay = wl.replay_H is not None
+    W_swa = [wl.w_swa(l).double().numpy() for l in range(len(wl.layers))] if replay else None
     # the sample: one sequence (the median-length one), its query tokens prepared once
     lens = [wl.entries_before(b) for b in range(wl.B)]
     b = sorted(range(wl.B), key=lambda x: lens[x])[wl.B // 2]
@@ -584,8 +597,15 @@ def cpu_worker(workload, seconds, ref_steps=0):
         L = len(wl.layers)
         qs = [(wl.idx_q_row(l, b, i).double().numpy(), wl.idx_w_row(l, b, i).double().numpy()) for l in range(L)]
         Qs = [wl.q_row(l, b, i).double().numpy() for l in range(L)]
-        win_pos = A.window_positions(t, wl.W)
-        win_lat = [wl.swa_latent(l, b, torch.from_numpy(win_pos)).numpy() for l in range(L)]
+        win_pos = OL.window_of(wl, b, t)
+        if replay:
+            # the window's other rows were rebuilt by the tokens before this one; this
+            # token rebuilds its own row inside the timed layer
+            k = win_pos - wl.t_first[b]
+            win_lat = [(st.replay_rows(l)["codes"][k], st.replay_rows(l)["scales"][k],
+                        wl.replay_hidden_rows(l, b)[i:i + 1].double().numpy()) for l in range(L)]
+        else:
+            win_lat = [wl.swa_latent(l, b, torch.from_numpy(win_pos)).numpy() for l in range(L)]
         # cached state: packed rows of every entry the schedule can gather (the Full
         # selection and, for the pooled indexer, every pooled position)
         sc = I.index_scores(qs[0][0], qs[0][1], Kall[:nv])
@@ -594,9 +614,9 @@ def cpu_worker(workload, seconds, ref_steps=0):
             cand.append(I.pool_positions(I.block_pool(sc, wl.pool_blocks, wl.pool_block), nv, wl.pool_block))
         cand = np.unique(np.concatenate(cand))
         c, s = st.packed_rows(cand)
-        prepared.append((nv, qs, Qs, win_lat, cand, c, s))
+        prepared.append((t, nv, qs, Qs, win_lat, cand, c, s))
 
-    def one_layer(l, state, nv, qs, Qs, win_lat, cand, c, s):
+    def one_layer(l, state, t, nv, qs, Qs, win_lat, cand, c, s):
         """Layer l of one query token; state carries the previous layer's indices and the pool."""
         mode = wl.layers[l]
         if mode == "F":
@@ -612,7 +632,13 @@ def cpu_worker(workload, seconds, ref_steps=0):
         state["prev"] = idx
         rows = np.searchsorted(cand, idx)
         kv = F.mxfp4_unpack(c[rows], s[rows])
-        wc, ws = F.fp8_pack(win_lat[l])
+        if replay:
+            wc, ws, own_h = win_lat[l]
+            own = R.window_rows(own_h, W_swa[l], st.gamma, wl.eps, wl.r, wl.rope_base, t)
+            wc, ws = wc.copy(), ws.copy()
+            wc[-1], ws[-1] = own["codes"][0], own["scales"][0]
+        else:
+            wc, ws = F.fp8_pack(win_lat[l])
         A.sparse_attention(Qs[l], kv, F.fp8_unpack_bf16(wc, ws), tau)
 
     L = len(wl.layers)
@@ -719,7 +745,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="decode",
                     choices=["decode", "prefill", "hierarchical", "ragged", "encoder_stack", "decoder_stack",
-                             "decoder_stack_prefill", "ced_compress"])
+                             "decoder_stack_prefill", "decoder_replay", "ced_compress"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -78,6 +78,9 @@ SIGNATURES = {
     "csa2_compress_layers_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32, _I32]),
     "csa2_compress_layers": (C.c_int, [_P, _I32, _I32, _I32, _I32, _P, _I32, _P, _F, _F, _P, C.POINTER(Dims),
                                        C.POINTER(Cache), _P, _SZ, _P]),
+    "csa2_swa_replay_workspace_size": (_SZ, [_I32, _I32, _I32, _I32]),
+    "csa2_swa_replay": (C.c_int, [_P, _I32, _I32, _I32, _P, _P, _F, _F, _P, C.POINTER(Dims), C.POINTER(Window),
+                                  _P, _SZ, _P]),
     "csa2_index_scores": (C.c_int, [C.POINTER(Dims), C.POINTER(Cache), _P, _P, _P, _P, _I64, _P, _I64, _P]),
     "csa2_topk_workspace_size": (_SZ, [_I64, _I64, _I32]),
     "csa2_topk_f32": (C.c_int, [_P, _I64, _I64, _P, _I32, _P, _P, _P, _SZ, _P]),
@@ -204,6 +207,18 @@ def csa2_compress_layers(hidden, W_all, Di, gamma_all, eps, rope_base, first_ent
                                       ptr(first_entry), C.byref(dims), arr, ptr(ws),
                                       ws.numel() * ws.element_size() if ws is not None else 0,
                                       stream_handle(stream)))
+
+
+def csa2_swa_replay_workspace_size(B, n_tok, H, d) -> int:
+    return lib().csa2_swa_replay_workspace_size(B, n_tok, H, d)
+
+
+def csa2_swa_replay(hidden, W_swa, gamma, eps, rope_base, tok_pos0, dims: Dims, window: Window, ws, stream=None):
+    """hidden [B][n_tok][H] bf16 of the replayed tokens; W_swa [d][H] bf16; tok_pos0 int32 [B]."""
+    B, n_tok, H = hidden.shape
+    _check(lib().csa2_swa_replay(ptr(hidden), B, n_tok, H, ptr(W_swa), ptr(gamma), eps, rope_base, ptr(tok_pos0),
+                                 C.byref(dims), C.byref(window), ptr(ws),
+                                 ws.numel() * ws.element_size() if ws is not None else 0, stream_handle(stream)))
 
 
 def csa2_index_scores(dims: Dims, cache: Cache, idx_q, w, q_pos, scores, blockmax=None, stream=None):

@@ -351,6 +351,43 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
   return CSA2_OK;
 }
 
+size_t csa2_swa_replay_workspace_size(int32_t B, int32_t n_tok, int32_t H, int32_t d) {
+  if (B <= 0 || n_tok <= 0 || H <= 0 || d <= 0) return 0;
+  return compress_partials_bytes(B, n_tok, H, d, 0, nullptr, 1);
+}
+
+int csa2_swa_replay(const uint16_t* hidden, int32_t B, int32_t n_tok, int32_t H, const uint16_t* W_swa,
+                    const float* gamma, float eps, float rope_base, const int32_t* tok_pos0, const csa2_dims* dm,
+                    const csa2_window* win, void* ws, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  int rc = check_dims(dm, false, false);
+  if (rc) return rc;
+  if (dm->d != 64 && dm->d != 512) return fail(CSA2_ERR_UNSUPPORTED, "d must be 64 or 512 (got %d)", dm->d);
+  REQUIRE(B == dm->B, "B (%d) must equal dims.B (%d)", B, dm->B);
+  REQUIRE(n_tok >= 0 && H > 0, "n_tok must be >= 0 and H > 0");
+  REQUIRE(H % 64 == 0, "H must be a multiple of 64 (got %d)", H);
+  REQUIRE(dm->r >= 0 && dm->r <= dm->d && dm->r % 2 == 0, "r must be even and in 0..d");
+  REQUIRE(eps >= 0.f, "eps must be >= 0");
+  if (B == 0 || n_tok == 0) return CSA2_OK;
+  REQUIRE_PTR(hidden); REQUIRE_PTR(W_swa); REQUIRE_PTR(gamma); REQUIRE_IPTR(tok_pos0);
+  REQUIRE(win, "window must not be NULL");
+  REQUIRE_PTR(win->codes); REQUIRE_PTR(win->scales); REQUIRE_IPTR(win->pos0);
+  REQUIRE(dm->swa_cap >= 1, "dims.swa_cap must be >= 1 (got %d)", dm->swa_cap);
+  int n_split = 1;
+  const size_t need = compress_partials_bytes(B, n_tok, H, dm->d, 0, &n_split, 1);
+  if (!ws || ws_bytes < need) return fail(CSA2_ERR_WORKSPACE, "swa_replay needs %zu workspace bytes (got %zu)", need, ws_bytes);
+  REQUIRE(aligned16(ws), "ws must be 16-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* part = static_cast<float*>(ws);
+  // one token per GEMM row: c_t = W_swa h_t, split-K fp32 partials
+  LAUNCH(launch_compress_gemm(hidden, B, n_tok, H, W_swa, dm->d, nullptr, 0, part, n_split, s, 1), "swa_replay_gemm");
+  LatentSource src{part, dm->d, (int64_t)B * n_tok * dm->d, n_split};
+  LAUNCH(launch_norm_rope_fp8_window(src, B, n_tok, dm->d, dm->r, gamma, eps, rope_base, tok_pos0, win->pos0,
+                                     dm->swa_cap, win->codes, win->scales, s),
+         "swa_replay_epilogue");
+  return CSA2_OK;
+}
+
 int csa2_index_scores(const csa2_dims* dm, const csa2_cache* c, const void* idx_q, const float* w,
                       const int32_t* q_pos, float* scores, int64_t score_stride, float* blockmax,
                       int64_t bm_stride, void* stream) {

@@ -1,9 +1,12 @@
 // 4:1 sequence compression: every 4 consecutive new tokens become one KV
 // entry through a learned linear map ("DeepSeek-V4.1 架构解析" §02; DeepSeek V4
 // review §2.1-§2.2), reading R1: c_j = W [h_4j; h_4j+1; h_4j+2; h_4j+3].
+// The same GEMM with one token per row projects the replayed tokens onto
+// their window rows (SWA Bounded Replay, §03; reading R13).
 //
-// The 4-token concatenation is a plain view of the row-major hidden states
-// (row j of A starts at token 4j), so A needs no gather.  The GEMM computes
+// The g-token concatenation (g = 4, or 1 for window rows) is a plain view of
+// the row-major hidden states (row j of A starts at token g j), so A needs no
+// gather.  The GEMM computes
 // [W; W_idx] (d + Di output channels) in one pass over A and writes split-K
 // fp32 partials; the epilogue kernel (pack.cu) sums the splits in a fixed
 // order, applies RMSNorm + RoPE + MXFP4 and stores the paged entry and its
@@ -51,11 +54,12 @@ __device__ __forceinline__ void g_mma(float (&d)[4], uint32_t a0, uint32_t a1, u
 // grid = (N tiles, M tiles, splits).  8 warps as 2 (M) x 4 (N), warp tile 64 x 32.
 __global__ void __launch_bounds__(kGThreads)
 k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const uint16_t* __restrict__ W,
-                int d, const uint16_t* __restrict__ W_idx, int Di, int M, float* __restrict__ partials) {
+                int d, const uint16_t* __restrict__ W_idx, int Di, int M, float* __restrict__ partials,
+                int tok_per_row) {
   __shared__ __align__(16) uint16_t sa[2][kGM * kGS];
   __shared__ __align__(16) uint16_t sb[2][kGN * kGS];
   const int N = d + Di;
-  const int64_t Kd = 4LL * H;
+  const int64_t Kd = (int64_t)tok_per_row * H;
   const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
   // split blockIdx.z of gridDim.z takes K steps [st0, st1)
   const int steps = (int)(Kd / kGK);
@@ -77,7 +81,7 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
     const int m = m0 + ld_row[i];
     a_ok[i] = m < M;
     const int mm = a_ok[i] ? m : 0;
-    a_src[i] = hidden + ((int64_t)(mm / G) * T + 4LL * (mm % G)) * H;
+    a_src[i] = hidden + ((int64_t)(mm / G) * T + (int64_t)tok_per_row * (mm % G)) * H;
     const int n = n0 + ld_row[i];
     b_ok[i] = n < N;
     b_src[i] = n < d ? W + (int64_t)n * Kd : W_idx + (int64_t)((b_ok[i] ? n : d) - d) * Kd;
@@ -148,8 +152,8 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
 // ---- tcgen05 + TMA path -------------------------------------------------------------
 // CTA tile 128 entries x 256 output channels; K in 64-wide stages of 48 KB
 // (A then B, both 128-byte-swizzled K-major) in a 4-stage ring filled by
-// tensor-map copies: A is the hidden states seen as [B][G][4H] (row j of
-// batch b starts at token 4j), B is W or W_idx (W_idx tiles hold Di rows;
+// tensor-map copies: A is the hidden states seen as [B][G][gH] (row j of
+// batch b starts at token g j), B is W or W_idx (W_idx tiles hold Di rows;
 // the tile's other columns are never stored).  Warp 0 issues the copies,
 // warp 1 the MMAs (M = 128, N = 256, K = 16) into a 256-column fp32
 // accumulator in tensor memory, warps 2..5 write the fp32 partial sums.
@@ -276,10 +280,11 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
 }
 
 // W_idx tiles start on a tile (d a multiple of 256); without W_idx any d >= 256 with
-// 16-byte rows of output works (the last tile's rows past d are zero-filled).
-static bool tma_compress_ok(int T, int H, int d, int Di) {
-  return (Di ? d % kTmN == 0 : (d >= kTmN && d % 4 == 0)) && H % 16 == 0 && T >= 4 && Di % 4 == 0 &&
-         Di <= kTmN && tensor_map_encoder() != nullptr;
+// 16-byte rows of output works (the last tile's rows past d are zero-filled).  The
+// K stages tile g H exactly.
+static bool tma_compress_ok(int T, int H, int d, int Di, int g) {
+  return (Di ? d % kTmN == 0 : (d >= kTmN && d % 4 == 0)) && H % 16 == 0 && (g * H) % kTmK == 0 && T >= g &&
+         Di % 4 == 0 && Di <= kTmN && tensor_map_encoder() != nullptr;
 }
 
 // Split K only as far as it takes to fill the SMs once.
@@ -289,8 +294,8 @@ static int compress_splits(int B, int G, int N, int Kd) {
   return (int)std::min<int64_t>(s, std::max(1, Kd / kTmK));
 }
 
-size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out) {
-  const int G = T / 4, M = B * G, N = d + Di, Kd = 4 * H;
+size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out, int g) {
+  const int G = T / g, M = B * G, N = d + Di, Kd = g * H;
   const int sp = compress_splits(B, G, N, Kd);
   if (n_split_out) *n_split_out = sp;
   return (size_t)sp * M * N * sizeof(float);
@@ -298,11 +303,11 @@ size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_
 
 cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, const uint16_t* W, int d,
                                  const uint16_t* W_idx, int Di, float* partials, int n_split,
-                                 cudaStream_t s) {
-  const int G = T / 4, M = B * G, N = d + (W_idx ? Di : 0), Kd = 4 * H;
+                                 cudaStream_t s, int g) {
+  const int G = T / g, M = B * G, N = d + (W_idx ? Di : 0), Kd = g * H;
   if (M == 0) return cudaSuccess;
-  if (tma_compress_ok(T, H, d, W_idx ? Di : 0)) {
-    // A: [B][G][4H] view of the hidden states; W: [d][4H]; W_idx: [Di][4H]
+  if (tma_compress_ok(T, H, d, W_idx ? Di : 0, g)) {
+    // A: [B][G][gH] view of the hidden states; W: [d][gH]; W_idx: [Di][gH]
     CUtensorMap amap, wmap, imap;
     const cuuint32_t estr[3] = {1, 1, 1};
     const cuuint64_t adims[3] = {(cuuint64_t)Kd, (cuuint64_t)G, (cuuint64_t)B};
@@ -332,7 +337,7 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
                        W_idx ? Di : 0, N, M, Kd / kTmK, n_split, partials, status_word());
   }
   dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
-  k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M, partials);
+  k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M, partials, g);
   return counted(cudaGetLastError());
 }
 

@@ -71,14 +71,22 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
                                   // optional indexer-key epilogue (compression)
                                   const float* idx_src, int64_t idx_row_stride, int Di,
                                   int idx_dtype, void* idx_k, cudaStream_t s);
+// Window rows rebuilt from replayed tokens: row i of sequence b (latent = the
+// split sum of src row b * n_tok + i) gets RMSNorm, RoPE at raw position
+// tok_pos0[b] + i and the FP8 pack, into window row tok_pos0[b] + i - win_pos0[b].
+cudaError_t launch_norm_rope_fp8_window(LatentSource src, int B, int n_tok, int d, int r,
+                                        const float* gamma, float eps, float rope_base,
+                                        const int32_t* tok_pos0, const int32_t* win_pos0, int swa_cap,
+                                        uint8_t* codes, float* scales, cudaStream_t s);
 
 // ---- compress.cu --------------------------------------------------------------
 // C[split][m][n] = sum over the split's K-range of A[m][:] * Bw[n][:], where
-// A rows are the 4-token groups of hidden and Bw = [W; W_idx] (n < d: W).
-size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out);
+// A rows are the g-token groups of hidden (g = 4: compression; g = 1: one
+// token per row, the window-row projection) and Bw = [W; W_idx] (n < d: W).
+size_t compress_partials_bytes(int B, int T, int H, int d, int Di, int* n_split_out, int g = 4);
 cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H,
                                  const uint16_t* W, int d, const uint16_t* W_idx, int Di,
-                                 float* partials, int n_split, cudaStream_t s);
+                                 float* partials, int n_split, cudaStream_t s, int g = 4);
 
 // ---- indexer.cu ---------------------------------------------------------------
 struct IndexerArgs {

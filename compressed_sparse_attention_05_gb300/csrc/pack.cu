@@ -100,23 +100,87 @@ __global__ void k_pack_fp8_window(const float* __restrict__ x, int B, int Tq, in
   fp8_row(x + row * d, d, codes + dst * d, scales + dst, threadIdx.x & 31);
 }
 
-// RMSNorm + RoPE + MXFP4 pack + paged store of one entry per warp.  Lane l
-// owns channels 16l .. 16l+15 (one MXFP4 group); d <= 512.
+// RMSNorm + RoPE of one latent row held by a warp.
 //
-// RoPE angles: position p = 4e + 3 reaches 4M, so the angle p * theta_i can
-// be ~4e6 rad.  The rotation of frequency i is kept as turns per position,
-// g_i = frac(theta_i / 2 pi) in 0.64 fixed point (host, fp64); p * g_i mod
-// 2^64 in integer arithmetic is then the angle's fraction of a turn (error
-// <= p * 2^-53 turns, like the fp64 product p * theta_i), and fp64 sincospi
-// of that fraction and an fp64 rotation give the rotated channels rounded
-// once to fp32, as an fp64 RoPE does: an fp32 rotation moves values across
-// the MXFP4 rounding boundaries now and then.  fp64 is slow on this GPU, so
-// the pairs are spread over the lanes: one angle and one pair per lane.
+// RoPE angles: the position p reaches ~4M (entry positions 4e + 3 of a 1M-entry
+// cache, or raw token positions), so the angle p * theta_i can be ~4e6 rad.
+// The rotation of frequency i is kept as turns per position, g_i =
+// frac(theta_i / 2 pi) in 0.64 fixed point (host, fp64); p * g_i mod 2^64 in
+// integer arithmetic is then the angle's fraction of a turn (error <= p *
+// 2^-53 turns, like the fp64 product p * theta_i), and fp64 sincospi of that
+// fraction and an fp64 rotation give the rotated channels rounded once to
+// fp32, as an fp64 RoPE does: an fp32 rotation moves values across the FP4 /
+// FP8 rounding boundaries now and then.  fp64 is slow on this GPU, so the
+// pairs are spread over the lanes: one angle and one pair per lane.
 constexpr int kNrpWarps = 4;
 struct RopeTurns {
   uint64_t g[256];   // r/2 <= 256 frequencies
 };
 
+// Lane l holds channels 16l .. 16l+15 of the row in v (has = 16l < d; d <= 512).
+// On return v holds the normalised, rotated channels and buf (the warp's row
+// buffer, d floats) the whole row.
+__device__ __forceinline__ void norm_rope_row(float (&v)[16], bool has, int d, int r,
+                                              const float* __restrict__ gamma, float eps, uint64_t pos,
+                                              const RopeTurns& rope, float* buf, int lane) {
+  float ss = 0.f;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) ss += v[c] * v[c];
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
+  if (has) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      v[c] = v[c] * inv * gamma[lane * 16 + c];
+      buf[lane * 16 + c] = v[c];
+    }
+  }
+  __syncwarp();
+  // rotate-half RoPE on channels [d - r, d): lane l rotates pair
+  // (d - r + l, d - r/2 + l) of each round of 32 pairs in the row buffer, then
+  // the channels' owners read them back
+  const int half = r / 2;
+  for (int k0 = 0; k0 < half; k0 += 32) {
+    const int pi = k0 + lane;
+    if (pi < half) {
+      double sn, cs;
+      const uint64_t turns = pos * rope.g[pi];                    // fraction of a turn, mod 2^64
+      sincospi((double)(int64_t)turns * 0x1p-63, &sn, &cs);       // angle / pi in [-1, 1)
+      const double x1 = (double)buf[d - r + pi], x2 = (double)buf[d - half + pi];
+      buf[d - r + pi] = (float)(x1 * cs - x2 * sn);
+      buf[d - half + pi] = (float)(x1 * sn + x2 * cs);
+    }
+  }
+  __syncwarp();
+  if (has && r > 0) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const int ch = lane * 16 + c;
+      if (ch >= d - r) v[c] = buf[ch];
+    }
+  }
+}
+
+// Lane l's 16 channels of latent row m: the split-K partials summed in a fixed
+// order (deterministic).
+__device__ __forceinline__ void load_latent(const LatentSource& src, int64_t m, bool has, int lane,
+                                            float (&v)[16]) {
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = 0.f;
+  if (!has) return;
+  for (int sp = 0; sp < src.n_split; ++sp) {
+    const float4* p = reinterpret_cast<const float4*>(src.base + sp * src.split_stride + m * src.row_stride +
+                                                      lane * 16);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float4 f = p[q];
+      v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
+    }
+  }
+}
+
+// RMSNorm + RoPE (at the entry position 4e + 3) + MXFP4 pack + paged store of
+// one entry per warp.  Lane l owns channels 16l .. 16l+15 (one MXFP4 group).
 __global__ void __launch_bounds__(kNrpWarps * 32)
 k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
                  float eps, float rope_base, const int32_t* __restrict__ first_entry,
@@ -136,60 +200,10 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
   const int64_t slot = entry_slot(page_table, max_pages, n_pages, b, e, status);
   if (slot < 0) return;
 
-  const int n_groups = d / 16;
-  const bool has = lane < n_groups;
+  const bool has = lane < d / 16;
   float v[16];
-#pragma unroll
-  for (int c = 0; c < 16; ++c) v[c] = 0.f;
-  if (has) {
-    for (int sp = 0; sp < src.n_split; ++sp) {   // fixed order: deterministic
-      const float4* p = reinterpret_cast<const float4*>(src.base + sp * src.split_stride +
-                                                        m * src.row_stride + lane * 16);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float4 f = p[q];
-        v[4 * q] += f.x; v[4 * q + 1] += f.y; v[4 * q + 2] += f.z; v[4 * q + 3] += f.w;
-      }
-    }
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int c = 0; c < 16; ++c) ss += v[c] * v[c];
-  ss = warp_sum(ss);
-  const float inv = 1.0f / sqrtf(ss / (float)d + eps);
-  if (has) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      v[c] = v[c] * inv * gamma[lane * 16 + c];
-      row_buf[warp][lane * 16 + c] = v[c];
-    }
-  }
-  __syncwarp();
-  // rotate-half RoPE on channels [d - r, d) at position 4e + 3, in fp64: lane
-  // l rotates pair (d - r + l, d - r/2 + l) of each round of 32 pairs in the
-  // row buffer, then the channels' owners read them back
-  const int half = r / 2;
-  const uint64_t pos = 4ull * (uint64_t)e + 3ull;
-  for (int k0 = 0; k0 < half; k0 += 32) {
-    const int pi = k0 + lane;
-    if (pi < half) {
-      double sn, cs;
-      const uint64_t turns = pos * rope.g[pi];                    // fraction of a turn, mod 2^64
-      sincospi((double)(int64_t)turns * 0x1p-63, &sn, &cs);       // angle / pi in [-1, 1)
-      float* x = row_buf[warp];
-      const double x1 = (double)x[d - r + pi], x2 = (double)x[d - half + pi];
-      x[d - r + pi] = (float)(x1 * cs - x2 * sn);
-      x[d - half + pi] = (float)(x1 * sn + x2 * cs);
-    }
-  }
-  __syncwarp();
-  if (has && r > 0) {
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const int ch = lane * 16 + c;
-      if (ch >= d - r) v[c] = row_buf[warp][ch];
-    }
-  }
+  load_latent(src, m, has, lane, v);
+  norm_rope_row(v, has, d, r, gamma, eps, 4ull * (uint64_t)e + 3ull, rope, row_buf[warp], lane);
   if (has) {
     Mxfp4Group g = pack_group16(v);
     reinterpret_cast<uint2*>(kv_codes + slot * (d / 2))[lane] = g.codes;
@@ -207,6 +221,38 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
         reinterpret_cast<float*>(idx_k)[slot * Di + c] = acc;
     }
   }
+}
+
+// Window rows of replayed tokens (SWA Bounded Replay, reading R13): one warp
+// per token sums its projection's split partials, applies RMSNorm and RoPE at
+// the token's own raw position and packs the row to FP8 (R5) into window row
+// tok_pos0[b] + i - win_pos0[b]; a row outside the buffer is skipped and
+// flagged.
+__global__ void __launch_bounds__(kNrpWarps * 32)
+k_norm_rope_fp8_window(LatentSource src, int B, int n_tok, int d, int r, const float* __restrict__ gamma,
+                       float eps, const int32_t* __restrict__ tok_pos0, const int32_t* __restrict__ win_pos0,
+                       int swa_cap, uint8_t* __restrict__ codes, float* __restrict__ scales,
+                       const __grid_constant__ RopeTurns rope, uint32_t* status) {
+  __shared__ __align__(16) float row_buf[kNrpWarps][512];
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
+  if (m >= (int64_t)B * n_tok) return;
+  const int b = (int)(m / n_tok), i = (int)(m % n_tok);
+  const int64_t p = (int64_t)tok_pos0[b] + i;
+  const int64_t wr = p - win_pos0[b];
+  if (p < 0 || wr < 0 || wr >= swa_cap) {
+    if (lane == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
+    return;
+  }
+  const bool has = lane < d / 16;
+  float v[16];
+  load_latent(src, m, has, lane, v);
+  norm_rope_row(v, has, d, r, gamma, eps, (uint64_t)p, rope, row_buf[warp], lane);
+  __syncwarp();
+  const int64_t dst = (int64_t)b * swa_cap + wr;
+  fp8_row(row_buf[warp], d, codes + dst * d, scales + dst, lane);
 }
 
 static inline unsigned grid_for(int64_t n, int per_block) {
@@ -245,6 +291,17 @@ cudaError_t launch_pack_fp8_window(const float* x, int B, int Tq, int d, const i
                      codes, scales, status_word());
 }
 
+// theta_i = base^(-2i/r) radians per position, as 0.64 fixed-point turns (host, fp64).
+static RopeTurns rope_turns(int r, float rope_base) {
+  RopeTurns rope = {};
+  for (int i = 0; i < r / 2; ++i) {
+    const double f = std::pow((double)rope_base, -2.0 * i / (double)r) / (2.0 * 3.14159265358979323846);
+    const double frac = std::ldexp(f - std::floor(f), 64);
+    rope.g[i] = frac >= 18446744073709551616.0 ? 0ull : (uint64_t)frac;
+  }
+  return rope;
+}
+
 cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r,
                                   const float* gamma, float eps, float rope_base,
                                   const int32_t* first_entry, const int32_t* n_rows,
@@ -255,15 +312,23 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
   const int64_t rows = (int64_t)B * n_max;
   if (rows == 0) return cudaSuccess;
   if (r < 0 || r / 2 > 256) return cudaErrorInvalidValue;
-  RopeTurns rope = {};
-  for (int i = 0; i < r / 2; ++i) {   // theta_i = base^(-2i/r) radians per position, as turns
-    const double f = std::pow((double)rope_base, -2.0 * i / (double)r) / (2.0 * 3.14159265358979323846);
-    const double frac = std::ldexp(f - std::floor(f), 64);
-    rope.g[i] = frac >= 18446744073709551616.0 ? 0ull : (uint64_t)frac;
-  }
+  const RopeTurns rope = rope_turns(r, rope_base);
   return launch_step(k_norm_rope_pack, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
       src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
       n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, rope, status_word());
+}
+
+cudaError_t launch_norm_rope_fp8_window(LatentSource src, int B, int n_tok, int d, int r,
+                                        const float* gamma, float eps, float rope_base,
+                                        const int32_t* tok_pos0, const int32_t* win_pos0, int swa_cap,
+                                        uint8_t* codes, float* scales, cudaStream_t s) {
+  const int64_t rows = (int64_t)B * n_tok;
+  if (rows == 0) return cudaSuccess;
+  if (r < 0 || r / 2 > 256 || d > 512 || d % 16 != 0) return cudaErrorInvalidValue;
+  const RopeTurns rope = rope_turns(r, rope_base);
+  return launch_step(k_norm_rope_fp8_window, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
+                     src, B, n_tok, d, r, gamma, eps, tok_pos0, win_pos0, swa_cap, codes, scales, rope,
+                     status_word());
 }
 
 }  // namespace csa2

@@ -9,8 +9,10 @@ include/csa2.h expects it, through the library's own kernels:
   per layer         Q, indexer q / w, window buffers, outputs
 
 Cached entries are written by csa2_norm_rope_pack from raw latent rows, window
-rows by csa2_pack_swa_fp8, so no packing happens outside the library.  The
-workload object (``wl``) supplies shapes and raw random tensors only.
+rows by csa2_pack_swa_fp8 (or, for a replay workload, by csa2_swa_replay from
+each layer's replayed hidden states inside the step), so no packing happens
+outside the library.  The workload object (``wl``) supplies shapes and raw
+random tensors only.
 """
 from __future__ import annotations
 
@@ -55,6 +57,14 @@ class LayerGroup:
         self.idx_q = [wl.idx_q(l, dev) if wl.layers[l] in "FX" else None for l in range(L)]
         self.idx_w = [wl.idx_w(l, dev) if wl.layers[l] in "FX" else None for l in range(L)]
         self.swa_pos0 = wl.swa_pos0().to(dev)
+        self.replay = wl.replay_H is not None
+        self.replay_hidden = self.W_swa = None
+        if self.replay:   # SWA Bounded Replay: every layer's window rebuilt from its replayed tokens
+            self.replay_hidden = [wl.replay_hidden(l, dev) for l in range(L)]
+            self.W_swa = [wl.w_swa(l, dev) for l in range(L)]
+            self.replay_pos0 = torch.tensor(wl.t_first, dtype=torch.int32, device=dev)
+            self.replay_ws = torch.empty(max(256, abi.csa2_swa_replay_workspace_size(B, wl.n_new, wl.replay_H, d)),
+                                         dtype=torch.uint8, device=dev)
         self.swa_codes, self.swa_scales, self.swa_new = [], [], []
         for l in range(L):
             codes = torch.zeros(B, wl.swa_cap, d, dtype=torch.uint8, device=dev)
@@ -67,6 +77,9 @@ class LayerGroup:
                     abi.csa2_pack_swa_fp8(lat, codes[b, :n], scales[b, :n])
             self.swa_codes.append(codes)
             self.swa_scales.append(scales)
+            if self.replay:
+                self.swa_new.append(None)
+                continue
             new = torch.stack([wl.swa_latent(l, b, self.q_pos[b].to(torch.int64)) for b in range(B)])
             self.swa_new.append(new.contiguous())
 
@@ -85,6 +98,8 @@ class LayerGroup:
         self.O = [torch.full((B, wl.Tq, wl.Hq, d), float("nan"), dtype=torch.float32, device=dev) for _ in range(L)]
         self.lse = [torch.full((B, wl.Tq, wl.Hq), float("nan"), dtype=torch.float32, device=dev) for _ in range(L)]
         self.args = [self._layer_args(l) for l in range(L)]
+        self._dims = self.dims()
+        self._windows = [self.window(l) for l in range(L)]
         ws = max(abi.csa2_layer_workspace_size(a) for a in self.args)
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev)
 
@@ -153,16 +168,26 @@ class LayerGroup:
         return a
 
     # -- the step ------------------------------------------------------------------------
+    def replay_window(self, l: int, stream=None):
+        """Rebuild layer l's window from its replayed tokens (SWA Bounded Replay)."""
+        wl = self.wl
+        abi.csa2_swa_replay(self.replay_hidden[l], self.W_swa[l], self.gamma, wl.eps, wl.rope_base,
+                            self.replay_pos0, self._dims, self._windows[l], self.replay_ws, stream)
+
     def step(self, layers: Optional[range] = None, stream=None):
         for l in (range(len(self.args)) if layers is None else layers):
+            if self.replay:
+                self.replay_window(l, stream)
             abi.csa2_layer(self.args[l], self.ws, stream)
 
     def step_inputs(self):
         """The per-step inputs a serving loop supplies (copied host->device in e2e runs)."""
         t = [*self.Q, *[x for x in self.idx_q if x is not None], *[x for x in self.idx_w if x is not None],
-             *self.swa_new]
+             *[x for x in self.swa_new if x is not None]]
         if self.hidden is not None:
             t.append(self.hidden)
+        if self.replay:
+            t.extend(self.replay_hidden)
         return t
 
     def step_outputs(self):

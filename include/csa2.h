@@ -81,6 +81,10 @@
  *      key in both sets counts twice.  O is fp32, lse (natural log) optional.
  *   R12 the indexer key of a new entry (Full layer with compression) is
  *      W_idx * [h_4j; ..; h_4j+3], rounded to the indexer dtype.
+ *   R13 SWA Bounded Replay (csa2_swa_replay): a rebuilt window row is the
+ *      replayed token's own latent RoPE_t(RMSNorm(W_swa h_t)) at its raw
+ *      position t, packed as R5; the rebuilt window starts at the first
+ *      replayed token.
  * ---------------------------------------------------------------------------
  */
 #ifndef CSA2_H
@@ -227,6 +231,30 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
                          const uint16_t* W_all, int32_t Di, const float* gamma_all, float eps,
                          float rope_base, const int32_t* first_entry, const csa2_dims* dims,
                          const csa2_cache* caches, void* ws, size_t ws_bytes, void* stream);
+
+/* ---- SWA Bounded Replay: a layer's window rebuilt from its last tokens -------
+ * "DeepSeek-V4.1 架构解析" §03 (SWA Bounded Replay): the window KV is not kept
+ * in the persistent cache; a layer rebuilds it by replaying only the last
+ * n_win (128) raw tokens, and tokens early in the replay see a shorter
+ * window than the exact state would give them.
+ * READING R13: the window row of raw token t is that token's own latent,
+ * x_t = RoPE_t(RMSNorm(W_swa h_t)): W_swa bf16 [d][H] without bias, R2's
+ * RMSNorm with gain gamma, R3's rotation at t itself (not at an entry
+ * position), then R5's FP8 pack.  With the window buffer's first row at the
+ * first replayed position, R11 gives a replayed token at p the rows
+ * max(first replayed position, p - W + 1) .. p.
+ * hidden bf16 [B][n_tok][H]: this layer's hidden states of the replayed
+ * tokens, row i of sequence b at raw position tok_pos0[b] + i (tok_pos0 int32
+ * [B], device); gamma fp32 [d].  Row i of sequence b is written to window
+ * row tok_pos0[b] + i - win->pos0[b]; a row outside [0, dims->swa_cap) is not
+ * written and raises CSA2_STATUS_BAD_COUNT.  Reads dims->B, d, r, swa_cap.
+ * Needs csa2_swa_replay_workspace_size() bytes of workspace.
+ * H: multiple of 64; d in {64, 512}. */
+size_t csa2_swa_replay_workspace_size(int32_t B, int32_t n_tok, int32_t H, int32_t d);
+int csa2_swa_replay(const uint16_t* hidden, int32_t B, int32_t n_tok, int32_t H, const uint16_t* W_swa,
+                    const float* gamma, float eps, float rope_base, const int32_t* tok_pos0,
+                    const csa2_dims* dims, const csa2_window* win, void* ws, size_t ws_bytes,
+                    void* stream);
 
 /* ---- a5: index scores of every visible entry (R6, R7) ----------------------
  * idx_q [B][Tq][Hi][Di] (idx_dtype), w fp32 [B][Tq][Hi], q_pos int32 [B][Tq].

@@ -134,3 +134,19 @@ def test_compress_layers_validation(lib):
     rc = lib.csa2_compress_layers(FAKE, 2, 64, 128, 2, FAKE, dm.Di, FAKE, 1e-6, 1e4, FAKE, C.byref(dm), caches,
                                   FAKE, need - 1, None)
     assert rc == 4
+
+
+def test_swa_replay_validation(lib):
+    win = abi.Window(codes=FAKE, scales=FAKE, pos0=FAKE)
+    call = lambda dims, H, n_tok, nbytes: lib.csa2_swa_replay(  # noqa: E731
+        FAKE, 2, n_tok, H, FAKE, FAKE, 1e-6, 1e4, FAKE, C.byref(dims), C.byref(win), FAKE, nbytes, None)
+    assert call(_dims(), 100, 128, 1 << 30) == 1 and "multiple of 64" in lib_err()
+    assert call(_dims(d=128), 128, 128, 1 << 30) == 2
+    assert call(_dims(swa_cap=0), 128, 128, 1 << 30) == 1 and "swa_cap" in lib_err()
+    assert call(_dims(B=3), 128, 128, 1 << 30) == 1 and "dims.B" in lib_err()
+    assert call(_dims(), 128, 0, 0) == 0          # nothing to replay: no launch, no workspace
+    need = abi.csa2_swa_replay_workspace_size(2, 128, 128, 512)
+    assert need > 0 and need % (2 * 128 * 512 * 4) == 0   # whole split-K partial planes
+    assert call(_dims(), 128, 128, need - 1) == 4
+    assert lib.csa2_swa_replay(FAKE, 2, 128, 128, FAKE, FAKE, 1e-6, 1e4, FAKE, C.byref(_dims()), None, FAKE,
+                               need, None) == 1 and "window" in lib_err()

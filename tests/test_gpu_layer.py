@@ -75,7 +75,7 @@ def check_group(wl, samples, group=None):
             prev = (gi, gc)
             # attention with the GPU's (verified) selection
             Q = _np(wl.q_row(l, b, i))
-            O, lse = A.sparse_attention(Q, st.kv_rows(gi[:gc]), st.swa_rows(l, A.window_positions(t, wl.W)), tau)
+            O, lse = A.sparse_attention(Q, st.kv_rows(gi[:gc]), st.swa_rows(l, OL.window_of(wl, b, t)), tau)
             err = parity.attn_err(g.O[l][b, i].cpu().numpy(), O)
             assert err <= parity.ATTN_RTOL, f"layer {l} ({mode}) token {(b, i)}: attention error {err}"
             # lse = log of the softmax normaliser; the kernels sum it from the fp32 or
@@ -158,6 +158,14 @@ def test_decoder_stack_prefill_small():
     (block maxima from the indexer GEMM), Reindex over the per-token pools."""
     wl = WL.decoder_stack_prefill(n_new=96, ctx=4096 + 96, H=256)
     check_group(wl, [(0, 0), (0, 33), (0, 95)])
+
+
+def test_decoder_replay_small():
+    """SWA Bounded Replay on the decoder schedule: every layer rebuilds its window
+    from its replayed tokens (csa2_swa_replay) and runs its step for them; the
+    first replayed token sees only itself in the window, the last a full one."""
+    wl = WL.decoder_replay(B=2, L=4 * 20000 + 40, n_win=40, H=256)
+    check_group(wl, [(0, 0), (0, 39), (1, 17)])
 
 
 def test_hierarchical_group_small():
