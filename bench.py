@@ -246,6 +246,9 @@ def run_gpu(args, rank, world, dist):
     # ---- dominant kernel, timed alone on the same stream through its own entry point
     kern = time_dominant_kernel(args, g, wl, flush, stream)
 
+    # ---- a replay step's own kernels: one layer's window rebuild, timed alone
+    replay = time_replay(args, g, wl, flush, stream) if wl.replay_H is not None else None
+
     # ---- end to end through the public call with host buffers
     e2e = time_e2e(args, g, flush, stream, dist)
 
@@ -273,6 +276,15 @@ def run_gpu(args, rank, world, dist):
         "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms),
         "clocks": clk.summary(),
     }
+    if replay is not None:
+        flops = 2 * wl.B * wl.Tq * wl.replay_H * wl.d
+        achieved = flops / (replay / 1e3) / 1e12
+        line["replay_roofline"] = {
+            "bound": "tensor", "kernel": "k_compress_gemm_tma (one token per row) + k_norm_rope_fp8_window",
+            "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": achieved / peaks["bf16_tflops"], "traffic": None, "algorithmic_flops_per_launch": flops,
+            "kernel_ms": replay, "peak_source": peaks["source"] + " (bf16 burst)",
+            "note": "one layer's csa2_swa_replay (projection GEMM + RMSNorm/RoPE/FP8 epilogue), L2 flushed"}
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -474,6 +486,25 @@ def time_dominant_kernel(args, g, wl, flush, stream):
         b.synchronize()
         tot += a.elapsed_time(b)
     return {"name": name, "ms": tot / n, "launches_timed": n}
+
+
+def time_replay(args, g, wl, flush, stream):
+    """Average duration (ms) of one layer's window rebuild (csa2_swa_replay), launched as
+    in the step, L2 flushed before each."""
+    import torch
+
+    n = max(3, min(args.steps, 200))
+    g.replay_window(0)
+    tot = 0.0
+    for k in range(n):
+        flush(k)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay_window(0)
+        b.record(stream)
+        b.synchronize()
+        tot += a.elapsed_time(b)
+    return tot / n
 
 
 def time_e2e(args, g, flush, stream, dist):
