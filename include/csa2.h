@@ -246,9 +246,10 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
  * hidden bf16 [B][n_tok][H]: this layer's hidden states of the replayed
  * tokens, row i of sequence b at raw position tok_pos0[b] + i (tok_pos0 int32
  * [B], device); gamma fp32 [d].  Row i of sequence b is written to window
- * row tok_pos0[b] + i - win->pos0[b]; a row outside [0, dims->swa_cap) is not
- * written and raises CSA2_STATUS_BAD_COUNT.  Reads dims->B, d, r, swa_cap.
- * Needs csa2_swa_replay_workspace_size() bytes of workspace.
+ * row tok_pos0[b] + i - win->pos0[b]; a row outside [0, dims->swa_cap), or at
+ * a negative raw position, is not written and raises CSA2_STATUS_BAD_COUNT.
+ * Uses dims->B, d, r and swa_cap (the struct is validated as for every entry
+ * point).  Needs csa2_swa_replay_workspace_size() bytes of workspace.
  * H: multiple of 64; d in {64, 512}. */
 size_t csa2_swa_replay_workspace_size(int32_t B, int32_t n_tok, int32_t H, int32_t d);
 int csa2_swa_replay(const uint16_t* hidden, int32_t B, int32_t n_tok, int32_t H, const uint16_t* W_swa,
