@@ -203,13 +203,32 @@ def committed_traffic(profile_md, src_path):
 def run_gpu(args, rank, world, dist):
     import torch
 
-    from compressed_sparse_attention_05_gb300 import abi, build, harness
+    from compressed_sparse_attention_05_gb300 import build
 
     build.build()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    line = measure(args, args.workload, args.steps, rank, world, dist, local)
+    # the metric's second configuration (prefill@64K) rides on the default decode line
+    if args.workload == "decode" and not args.no_prefill:
+        sub = measure(args, "prefill", max(3, min(args.steps, 400)), rank, world, dist, local)
+        if sub is not None:
+            for k in ("metric", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "dtype", "data"):
+                sub.pop(k, None)
+            line["prefill"] = sub
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure(args, workload, steps, rank, world, dist, local):
+    """Times `steps` steps of one workload (after args.warmup warm-up steps) and returns
+    its JSON object on rank 0 (None elsewhere)."""
+    import torch
+
+    from compressed_sparse_attention_05_gb300 import abi, harness
+
     dev = torch.device("cuda", local)
-    wl = make_workload(args.workload)
+    wl = make_workload(workload)
     wl.seed = replica_seed(wl.seed, rank)
     alg = algorithmic(wl)
     g = harness.LayerGroup(wl, f"cuda:{local}")
@@ -228,11 +247,11 @@ def run_gpu(args, rank, world, dist):
     assert abi.csa2_get_status() == 0
 
     # ---- headline: K steps, inputs resident, L2 flushed before each
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier()
     n0 = abi.csa2_launch_count()
     with ClockSampler(local) as clk:
-        for k in range(args.steps):
+        for k in range(steps):
             flush(k)
             ev[k][0].record(stream)
             g.step()
@@ -240,7 +259,7 @@ def run_gpu(args, rank, world, dist):
         barrier()
     launches = abi.csa2_launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / args.steps
+    ms = sum(step_ms) / steps
     ms_all = max_over_ranks(ms, dist, dev)
 
     # ---- dominant kernel, timed alone on the same stream through its own entry point
@@ -254,13 +273,13 @@ def run_gpu(args, rank, world, dist):
 
     status = abi.csa2_get_status()
     if rank != 0:
-        return
+        return None
     tokens = wl.B * wl.Tq
     value = world * tokens / (ms_all / 1e3)
     peaks = load_peaks()
     roof = roofline(wl, alg, kern, peaks)
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": tokens,
@@ -286,8 +305,8 @@ def run_gpu(args, rank, world, dist):
             "kernel_ms": replay, "peak_source": peaks["source"] + " (bf16 burst)",
             "note": "one layer's csa2_swa_replay (projection GEMM + RMSNorm/RoPE/FP8 epilogue), L2 flushed"}
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
-    print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline_all(workload, args.cpu_seconds)
+    return line
 
 
 # ---------------------------------------------------------------------------------
@@ -409,7 +428,7 @@ def run_ced(args, rank, world, dist):
         "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms), "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline("ced_compress", args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline_all("ced_compress", args.cpu_seconds)
     print(json.dumps(line), flush=True)
 
 
@@ -583,18 +602,52 @@ def step_roofline(wl, alg, ms, peaks):
 # ---------------------------------------------------------------------------------
 # the CPU oracle on a bounded sample
 
+def _cpu_cmd(workload, seconds, ref_steps, part=0):
+    return [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-worker", "--workload", workload,
+            "--cpu-seconds", str(seconds), "--ref-steps", str(ref_steps), "--cpu-part", str(part)]
+
+
+_CPU_ENV = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                CUDA_VISIBLE_DEVICES="")
+
+
 def cpu_baseline(workload, seconds, ref_steps=0):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-worker", "--workload", workload,
-           "--cpu-seconds", str(seconds), "--ref-steps", str(ref_steps)]
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(600, 20 * seconds))
+    """The oracle in one single-threaded worker process."""
+    r = subprocess.run(_cpu_cmd(workload, seconds, ref_steps), capture_output=True, text=True, env=_CPU_ENV,
+                       timeout=max(600, 20 * seconds))
     if r.returncode != 0:
         return {"error": r.stderr[-500:]}
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_worker(workload, seconds, ref_steps=0):
+def cpu_baseline_all(workload, seconds):
+    """The oracle on every host core: one single-threaded worker per core, each on its own
+    query tokens, run at the same time; throughput = the workers' sum.  The single-thread
+    run is reported beside it."""
+    single = cpu_baseline(workload, seconds)
+    n = os.cpu_count() or 1
+    procs = [subprocess.Popen(_cpu_cmd(workload, seconds, 0, part=p), stdout=subprocess.PIPE,
+                              stderr=subprocess.PIPE, text=True, env=_CPU_ENV) for p in range(n)]
+    vals, err = [], None
+    for p in procs:
+        try:
+            out, e = p.communicate(timeout=max(600, 30 * seconds))
+        except subprocess.TimeoutExpired:
+            p.kill()
+            out, e = p.communicate()
+        if p.returncode != 0:
+            err = e[-300:]
+            continue
+        vals.append(json.loads(out.strip().splitlines()[-1]))
+    if not vals:
+        return {"error": err, "single_thread": single}
+    return {"value": sum(v["value"] for v in vals), "unit": "tokens/s", "cores": len(vals), "kind": "oracle",
+            "sample": f"{len(vals)} single-threaded float64 numpy workers at once (one per host core, "
+                      f"os.cpu_count() = {n}), each: {vals[0]['sample']}; throughput summed",
+            "single_thread": single}
+
+
+def cpu_worker(workload, seconds, ref_steps=0, part=0):
     """Times the oracle's arithmetic for whole query tokens of the workload (inputs and
     cached state prepared outside the timer), single-threaded.
 
@@ -616,13 +669,14 @@ def cpu_worker(workload, seconds, ref_steps=0):
     tau = 1.0 / math.sqrt(wl.d)
     replay = wl.replay_H is not None
     W_swa = [wl.w_swa(l).double().numpy() for l in range(len(wl.layers))] if replay else None
-    # the sample: one sequence (the median-length one), its query tokens prepared once
+    # the sample: one sequence (the median-length one; worker `part` of an all-cores run
+    # takes the part-th sequence around it), its query tokens prepared once
     lens = [wl.entries_before(b) for b in range(wl.B)]
-    b = sorted(range(wl.B), key=lambda x: lens[x])[wl.B // 2]
+    b = sorted(range(wl.B), key=lambda x: lens[x])[(wl.B // 2 + part) % wl.B]
     st = OL.SequenceState(wl, b)
     Kall = st.indexer_keys()
     prepared = []
-    for i in ([0] if wl.Tq == 1 else [0, wl.Tq // 2, wl.Tq - 1]):
+    for i in ([0] if wl.Tq == 1 else [(j + 37 * part) % wl.Tq for j in (0, wl.Tq // 2, wl.Tq - 1)]):
         t = wl.t_first[b] + i
         nv = I.n_visible(Kall.shape[0], t)
         L = len(wl.layers)
@@ -783,13 +837,16 @@ def main():
                     help="CPU budget of the whole reference run, shared out over warmup + steps")
     ap.add_argument("--ref-steps", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="default decode run: skip the prefill@64K object")
+    ap.add_argument("--cpu-part", type=int, default=0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-worker", action="store_true")
     args = ap.parse_args()
     if args.cpu_worker:
         if args.workload == "ced_compress":
             ced_cpu_worker(args.cpu_seconds, args.ref_steps)
         else:
-            cpu_worker(args.workload, args.cpu_seconds, args.ref_steps)
+            cpu_worker(args.workload, args.cpu_seconds, args.ref_steps, args.cpu_part)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

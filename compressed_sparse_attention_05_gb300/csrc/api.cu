@@ -3,6 +3,7 @@
 // kernels.  Nothing here allocates device memory or synchronises a stream
 // (except csa2_get_status, which reads the status word back).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -19,6 +20,14 @@ __device__ uint32_t g_status_word;
 
 static thread_local char g_err[512];
 
+// NVTX range over one entry point (its validation and kernel launches), so that a
+// profiler timeline groups each launch under the call that made it.  Costs a
+// function call when no tool is attached.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 static int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -31,18 +40,61 @@ static int cuda_fail(cudaError_t e, const char* what) {
   return fail(CSA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-uint32_t* status_word() {
-  static std::mutex mu;
-  static uint32_t* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
+// Unique id of the calling thread's current CUDA context (0 if there is none).
+// Module globals (the status word, the no-allocation scratch) get a new
+// device address whenever the context is re-created (cudaDeviceReset), so
+// their cached addresses are keyed on this id rather than on the device
+// ordinal.  The driver calls are reached through the runtime (no libcuda link).
+static unsigned long long current_context_id() {
+  using GetCurrent = int (*)(void**);
+  using GetId = int (*)(void*, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<uint32_t*>(p);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(p);
+  });
+  void* ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != 0 || !ctx || get_id(ctx, &id) != 0) return 0;
+  return id;
+}
+
+void* symbol_address_cached(const void* symbol, cudaError_t* err) {
+  static std::mutex mu;
+  struct Entry {
+    unsigned long long ctx;
+    const void* symbol;
+    void* addr;
+  };
+  static Entry cache[128];
+  static int n = 0;
+  *err = cudaSuccess;
+  const unsigned long long ctx = current_context_id();
+  std::lock_guard<std::mutex> lock(mu);
+  if (ctx)
+    for (int i = 0; i < n; ++i)
+      if (cache[i].ctx == ctx && cache[i].symbol == symbol) return cache[i].addr;
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, symbol);
+  if (*err != cudaSuccess) return nullptr;
+  if (ctx) {
+    const int slot = n < 128 ? n++ : (int)(ctx % 128);
+    cache[slot] = Entry{ctx, symbol, p};
   }
-  return addr[dev];
+  return p;
+}
+
+uint32_t* status_word() {
+  cudaError_t e;
+  return static_cast<uint32_t*>(symbol_address_cached(reinterpret_cast<const void*>(&g_status_word), &e));
 }
 
 static std::atomic<uint64_t> g_launches{0};
@@ -186,6 +238,7 @@ int csa2_get_status(uint32_t* bits, void* stream) {
 
 int csa2_pack_mxfp4_f32(const float* x, int64_t n_rows, int32_t d, uint8_t* codes, uint8_t* scales,
                         void* stream) {
+  NvtxRange nvtx_("csa2_pack_mxfp4_f32");
   g_err[0] = 0;
   REQUIRE(n_rows >= 0, "n_rows must be >= 0");
   REQUIRE(d > 0 && d % 16 == 0 && d <= 4096, "d must be a multiple of 16 in 16..4096 (got %d)", d);
@@ -197,6 +250,7 @@ int csa2_pack_mxfp4_f32(const float* x, int64_t n_rows, int32_t d, uint8_t* code
 
 int csa2_unpack_mxfp4_bf16(const uint8_t* codes, const uint8_t* scales, int64_t n_rows, int32_t d,
                            uint16_t* out, void* stream) {
+  NvtxRange nvtx_("csa2_unpack_mxfp4_bf16");
   g_err[0] = 0;
   REQUIRE(n_rows >= 0, "n_rows must be >= 0");
   REQUIRE(d > 0 && d % 16 == 0 && d <= 4096, "d must be a multiple of 16 in 16..4096 (got %d)", d);
@@ -208,6 +262,7 @@ int csa2_unpack_mxfp4_bf16(const uint8_t* codes, const uint8_t* scales, int64_t 
 
 int csa2_pack_swa_fp8(const float* x, int64_t n_rows, int32_t d, uint8_t* codes, float* scales,
                       void* stream) {
+  NvtxRange nvtx_("csa2_pack_swa_fp8");
   g_err[0] = 0;
   REQUIRE(n_rows >= 0, "n_rows must be >= 0");
   REQUIRE(d > 0 && d % 16 == 0 && d <= 4096, "d must be a multiple of 16 in 16..4096 (got %d)", d);
@@ -221,6 +276,7 @@ int csa2_norm_rope_pack(const float* latent, int32_t B, int32_t n_max, int32_t d
                         const float* gamma, float eps, float rope_base, const int32_t* first_entry,
                         const int32_t* n_rows, const int32_t* page_table, int32_t max_pages,
                         int64_t n_pages, uint8_t* kv_codes, uint8_t* kv_scales, void* stream) {
+  NvtxRange nvtx_("csa2_norm_rope_pack");
   g_err[0] = 0;
   REQUIRE(B >= 0 && n_max >= 0, "B and n_max must be >= 0");
   if (d != 64 && d != 512) return fail(CSA2_ERR_UNSUPPORTED, "d must be 64 or 512 (got %d)", d);
@@ -259,6 +315,7 @@ int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, 
                        const float* gamma, float eps, float rope_base, const uint16_t* W_idx,
                        const int32_t* first_entry, const csa2_dims* dm, const csa2_cache* c, void* ws,
                        size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_compress_pack");
   g_err[0] = 0;
   int rc = check_dims(dm, false, false);
   if (rc) return rc;
@@ -297,6 +354,7 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
                          const uint16_t* W_all, int32_t Di, const float* gamma_all, float eps, float rope_base,
                          const int32_t* first_entry, const csa2_dims* dm, const csa2_cache* caches, void* ws,
                          size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_compress_layers");
   g_err[0] = 0;
   int rc = check_dims(dm, false, false);
   if (rc) return rc;
@@ -359,6 +417,7 @@ size_t csa2_swa_replay_workspace_size(int32_t B, int32_t n_tok, int32_t H, int32
 int csa2_swa_replay(const uint16_t* hidden, int32_t B, int32_t n_tok, int32_t H, const uint16_t* W_swa,
                     const float* gamma, float eps, float rope_base, const int32_t* tok_pos0, const csa2_dims* dm,
                     const csa2_window* win, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_swa_replay");
   g_err[0] = 0;
   int rc = check_dims(dm, false, false);
   if (rc) return rc;
@@ -391,6 +450,7 @@ int csa2_swa_replay(const uint16_t* hidden, int32_t B, int32_t n_tok, int32_t H,
 int csa2_index_scores(const csa2_dims* dm, const csa2_cache* c, const void* idx_q, const float* w,
                       const int32_t* q_pos, float* scores, int64_t score_stride, float* blockmax,
                       int64_t bm_stride, void* stream) {
+  NvtxRange nvtx_("csa2_index_scores");
   g_err[0] = 0;
   int rc = check_dims(dm, true, false);
   if (rc) return rc;
@@ -419,6 +479,7 @@ size_t csa2_topk_workspace_size(int64_t rows, int64_t stride, int32_t k) {
 
 int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32_t* n_valid, int32_t k,
                   int32_t* out_idx, int32_t* out_cnt, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_topk_f32");
   (void)ws; (void)ws_bytes;
   g_err[0] = 0;
   REQUIRE(rows >= 0 && rows < (1LL << 31), "rows out of range");
@@ -452,6 +513,7 @@ int csa2_topk_f32(const float* scores, int64_t rows, int64_t stride, const int32
 int csa2_block_pool_f32(const float* scores, int64_t rows, int64_t stride, const int32_t* n_valid,
                         int32_t block, int32_t n_pool_blocks, int32_t* out_pool, int32_t* out_pool_cnt,
                         float* out_blockmax, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_block_pool_f32");
   g_err[0] = 0;
   REQUIRE(rows >= 0 && rows < (1LL << 31), "rows out of range");
   REQUIRE(stride >= 1 && stride < (1LL << 31), "stride out of range");
@@ -571,6 +633,7 @@ int csa2_index_topk(const csa2_dims* dm, const csa2_cache* c, const void* idx_q,
                     const int32_t* q_pos, const int32_t* pool, const int32_t* pool_cnt, int32_t* out_idx,
                     int32_t* out_cnt, int32_t* out_pool, int32_t* out_pool_cnt, int32_t max_entries,
                     void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_index_topk");
   g_err[0] = 0;
   return index_topk_impl(dm, c, idx_q, w, q_pos, pool, pool_cnt, out_idx, out_cnt, out_pool, out_pool_cnt,
                          max_entries, ws, ws_bytes, static_cast<cudaStream_t>(stream));
@@ -603,6 +666,7 @@ static int attn_impl(const csa2_dims* dm, const csa2_cache* c, const csa2_window
 int csa2_sparse_attn(const csa2_dims* dm, const csa2_cache* c, const csa2_window* win, const uint16_t* Q,
                      const int32_t* q_pos, const int32_t* idx, const int32_t* cnt, float softmax_scale,
                      float* O, float* lse, void* stream) {
+  NvtxRange nvtx_("csa2_sparse_attn");
   g_err[0] = 0;
   return attn_impl(dm, c, win, Q, q_pos, idx, cnt, softmax_scale, O, lse, static_cast<cudaStream_t>(stream));
 }
@@ -619,6 +683,7 @@ size_t csa2_layer_workspace_size(const csa2_layer_args* a) {
 }
 
 int csa2_layer(const csa2_layer_args* a, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx_("csa2_layer");
   g_err[0] = 0;
   REQUIRE(a, "args must not be NULL");
   REQUIRE(a->mode == CSA2_MODE_FULL || a->mode == CSA2_MODE_REINDEX || a->mode == CSA2_MODE_REUSE,

@@ -5,7 +5,8 @@
 // 128 tokens).  Same result as the legacy kernels of attention.cu: head
 // layout, key set and softmax follow reading R11 of include/csa2.h.
 //
-// Shapes: d = 512, up to 64 query heads, up to 1,024 keys per token.  The
+// Shapes: d = 512, up to 128 query heads (one CTA per group of 64), up to
+// 3,072 keys per token (K <= 2,048 plus W <= 1,024).  The
 // token's key list (selected entries, then window rows) is cut into chunks
 // of 128 keys.  Swapped operands put the 128 keys of a chunk, not the 64
 // heads, on the MMA's M side:
@@ -35,10 +36,17 @@
 // up to 8 CTAs; each CTA finishes a partial (m, l, O) and the cluster merges
 // them through distributed shared memory, without global scratch.
 //
-// Operands are fp16: MXFP4 values (<= 6 significant bits, in [2^-10, 2688])
-// exact, bf16 Q and bf16-rounded window values exact in the fp16 range.  P is
-// rounded to fp16 for the PV product; the normaliser sums the unrounded fp32
-// P (relative difference <= 2^-11).  Accumulation is fp32.
+// Operands are fp16.  MXFP4 values (<= 6 significant bits, in [2^-10, 2688])
+// are exact.  bf16 values outside fp16's range are brought into it by powers
+// of two, which change no bit of a significand: each head of Q is scaled by
+// 2^-e_h so that its largest magnitude lies in [2^14, 2^15) (and its logits
+// are multiplied back by 2^e_h), and a window row whose per-token scale lies
+// outside [2^-8, 2^7] is dequantised with the scale 2^-f s (s' in [1, 2)), its
+// logits multiplied back by 2^f and its softmax weight carried as 2^f p in the
+// PV product (the reference maximum then follows the largest 2^f p, and the
+// normaliser adds p itself).  P is rounded to fp16 for the PV product; the
+// normaliser sums the unrounded fp32 P (relative difference <= 2^-11).
+// Accumulation is fp32.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -53,7 +61,8 @@ namespace {
 constexpr int kD = 512;          // latent width (keys = values)
 constexpr int kHeads = 64;       // N of both products; fewer heads are zero-padded
 constexpr int kChunk = 128;      // keys per chunk (M of the score product)
-constexpr int kMaxChunks = 8;    // keys per token <= 1,024; also the largest portable cluster
+constexpr int kMaxChunks = 24;   // keys per token <= 3,072 (K <= 2,048 plus W <= 1,024)
+constexpr int kMaxSplit = 8;     // CTAs per token in the cluster path (largest portable cluster)
 constexpr int kWorkers = 512;             // 16 warps: dequantisation and softmax
 constexpr int kThreads = kWorkers + 32;   // + one warp that allocates tensor memory and issues the MMAs
 constexpr uint32_t kTmemCols = 512;
@@ -71,7 +80,10 @@ struct TcSmem {
   uint16_t k[kChunk * kD];             // becomes the fp32 partial O [64][512] in the cluster merge
   uint16_t p[kChunk * kHeads];
   int32_t slot[kMaxChunks * kChunk];   // >= 0 main-KV slot; <= -2 window row (-2 - row); -1 none
+  int8_t kexp[kMaxChunks * kChunk];    // window row: exponent f of its dequantisation scale (0: none)
   float red[4][kHeads];                // per lane-quarter partial max / sum
+  float sl2h[kHeads];                  // logit multiplier of each head: softmax scale * log2(e) * 2^e_h
+  int qexp[kHeads];                    // largest bf16 exponent field of each head of Q
   float m_ref[kHeads];                 // reference maximum (log2 domain) of each head
   float m_thr[kHeads];                 // m_ref + 2^8 growth allowance
   float m_exp[kHeads];                 // m_ref, or 0 while the head has seen no key
@@ -218,8 +230,11 @@ __device__ __forceinline__ void load_slice(const AttnArgs& a, int32_t src, int q
   if (src >= 0)
     kb.v[SL] = __ldg(reinterpret_cast<const uint4*>(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL));
 }
+// Dequantisation scale of a window row, times 2^-f (see window_exp).
 __device__ __forceinline__ float load_wscale(const AttnArgs& a, int32_t src) {
-  return src <= -2 ? __ldg(a.swa_scales + (-2 - (int64_t)src)) : 0.f;
+  if (src > -2) return 0.f;
+  const float sw = __ldg(a.swa_scales + (-2 - (int64_t)src));
+  return sw * pow2i(-window_exp(sw));
 }
 
 // Dequantise the thread's 32 dims of slice SL into the K tile (4 core-matrix rows).
@@ -282,14 +297,26 @@ __device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, in
   return -1;
 }
 
-// Scores of the thread's key for heads 16*hg .. +15, in the log2 domain
-// (S^T times scale*log2(e)), or -inf for a missing key.
-__device__ __forceinline__ void load_scores(uint32_t tm, int hg, uint32_t lane_q, bool valid, float sl2,
-                                            float (&x)[16]) {
+// Scores of the thread's key for heads 16*hg .. +15 in the log2 domain, as
+// the PV product carries them: y = x + f with x = S^T * scale * log2(e) (the
+// head's and the key's powers of two undone), or -inf for a missing key.
+__device__ __forceinline__ void load_scores(uint32_t tm, int hg, uint32_t lane_q, bool valid, const float* sl2h,
+                                            int fk, float (&x)[16]) {
   tc::tmem_ld16(tm + kColS + 16 * hg + lane_q, x);
   tc::tmem_wait_ld();
+  const float4* m4 = reinterpret_cast<const float4*>(sl2h + 16 * hg);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] * sl2 : -INFINITY;
+  for (int j4 = 0; j4 < 4; ++j4) {
+    const float4 m = m4[j4];
+    x[4 * j4] *= m.x; x[4 * j4 + 1] *= m.y; x[4 * j4 + 2] *= m.z; x[4 * j4 + 3] *= m.w;
+  }
+  if (fk != 0) {   // a rescaled window row: logits times 2^f, weights carried as 2^f p
+    const float kf = pow2i(fk), ff = (float)fk;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = x[j] * kf + ff;
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = valid ? x[j] : -INFINITY;
 }
 
 // Bounded wait of a whole warp; on time-out the CTA's abort flag is raised.
@@ -316,6 +343,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   const int64_t row = blockIdx.x / n_split;
   const int rank = (int)(blockIdx.x % n_split);
   const int b = (int)(row / a.Tq);
+  const int hb = kHeads * (int)blockIdx.y;   // first head of this CTA's group of 64
   // dequantisation: one key, 32 dims of each slice.  A warp holds 8 whole keys
   // (coalesced loads); lanes 8q .. 8q+7 hold quarter q of the 8 keys, so each
   // 8-lane phase of a 16-byte store covers 8 distinct bank groups.
@@ -334,7 +362,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   for (int r = 0; r < 8; ++r) {
     const int u = tid + kWorkers * r;
     const int h = ((u >> 9) << 3) | (u & 7), c8 = (u >> 3) & 63;
-    qv[r] = (!mma_warp && h < a.Hq) ? __ldg(reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + h) * kD + c8 * 8))
+    qv[r] = (!mma_warp && hb + h < a.Hq) ? __ldg(reinterpret_cast<const uint4*>(a.Q + (row * a.Hq + hb + h) * kD + c8 * 8))
                                     : make_uint4(0, 0, 0, 0);
   }
   if (tid == 0) {
@@ -352,18 +380,44 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     sm.m_ref[tid] = -INFINITY;
     sm.m_thr[tid] = -INFINITY;
     sm.m_exp[tid] = 0.f;
+    sm.qexp[tid] = 0;
   }
-  // Q (bf16) -> fp16 B operand
+  __syncthreads();
+  // largest bf16 exponent field of each head (lanes L, L^8, L^16, L^24 share a head)
+  if (!mma_warp) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      uint32_t e = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t w = word_of(qv[r], j);
+        e = max(e, max((w >> 7) & 0xFFu, (w >> 23) & 0xFFu));
+      }
+      e = max(e, __shfl_xor_sync(0xffffffffu, e, 8));
+      e = max(e, __shfl_xor_sync(0xffffffffu, e, 16));
+      if (lane < 8 && e) atomicMax(&sm.qexp[8 * r + lane], (int)e);
+    }
+  }
+  __syncthreads();
+  // per head: 2^-e_h brings the largest magnitude into [2^14, 2^15) (e_h in [-110, 110])
+  if (tid < kHeads) {
+    const int eh = q_head_exp(sm.qexp[tid]);
+    sm.qexp[tid] = eh;
+    sm.sl2h[tid] = a.scale * 1.4426950408889634f * pow2i(eh);
+  }
+  __syncthreads();
+  // Q (bf16) -> fp16 B operand, head h scaled by 2^-e_h (exact)
   if (!mma_warp) {
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
       const int u = tid + kWorkers * r;
       const int h = ((u >> 9) << 3) | (u & 7), c8 = (u >> 3) & 63;
+      const float qs = pow2i(-sm.qexp[h]);
       uint32_t ov[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t w = word_of(qv[r], j);
-        ov[j] = f32x2_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+        ov[j] = f32x2_f16x2(__uint_as_float(w << 16) * qs, __uint_as_float(w & 0xFFFF0000u) * qs);
       }
       *reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(sm.q) + (h >> 3) * 8192 + c8 * 128 + (h & 7) * 16) =
           make_uint4(ov[0], ov[1], ov[2], ov[3]);
@@ -391,10 +445,16 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   int32_t cur_src = -1;
   if (!mma_warp && n_my > 0) {
     cur_src = key_source(a, row, b, c0 * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, qd == 0, status);
-    if (qd == 0) sm.slot[key] = cur_src;
-    for (int c = qd + 1; c < n_my; c += 4)
-      sm.slot[c * kChunk + key] =
+    if (qd == 0) {
+      sm.slot[key] = cur_src;
+      sm.kexp[key] = (int8_t)(cur_src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)cur_src))) : 0);
+    }
+    for (int c = qd + 1; c < n_my; c += 4) {
+      const int32_t src =
           key_source(a, row, b, (c0 + c) * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, true, status);
+      sm.slot[c * kChunk + key] = src;
+      sm.kexp[c * kChunk + key] = (int8_t)(src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)src))) : 0);
+    }
   }
   // ---- the first chunk's packed bytes
   float cur_wsc = 0.f;
@@ -452,7 +512,6 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   } else {
     // ================= workers: dequantisation and softmax =================
     unsigned char* ktile = reinterpret_cast<unsigned char*>(sm.k);
-    const float sl2 = a.scale * 1.4426950408889634f;
     const uint32_t lane_q = (uint32_t)(32 * q4) << 16;
     const int kc = 32 * q4 + lane;   // the softmax thread's key
     float lsum[16];
@@ -490,6 +549,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
         load_slice<3>(a, nxt_src, qd, kb);
       }
       const bool valid = sm.slot[it * kChunk + kc] != -1;   // the softmax thread's key
+      const int fk = sm.kexp[it * kChunk + kc];
       cur_src = nxt_src;
       cur_wsc = load_wscale(a, nxt_src);
       cur_sc = load_scales(a, nxt_src, qd);
@@ -500,7 +560,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       float x[16];
       bool above = false;
       if (wok) {
-        load_scores(tm, hg, lane_q, valid, sl2, x);
+        load_scores(tm, hg, lane_q, valid, sm.sl2h, fk, x);
         const float4* thr = reinterpret_cast<const float4*>(&sm.m_thr[16 * hg]);
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
@@ -516,7 +576,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
         // reduce the chunk's maxima (x is consumed, then summed again from tensor memory)
         const float mx = reduce16<true>(x, lane);
         if (lane < 16) sm.red[q4][16 * hg + lane] = mx;
-        load_scores(tm, hg, lane_q, valid, sl2, x);
+        load_scores(tm, hg, lane_q, valid, sm.sl2h, fk, x);
         workers_sync();
         int need = 0;
         if (tid < kHeads) {
@@ -555,16 +615,17 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       // P = exp2(s - m_ref) in fp16 (the MN-major B operand of the PV product)
       {
         uint32_t pk[8];
+        const float pf = pow2i(-fk);   // the normaliser adds p = 2^-f (2^f p)
         const float4* me = reinterpret_cast<const float4*>(&sm.m_exp[16 * hg]);
 #pragma unroll
         for (int j4 = 0; j4 < 4; ++j4) {
           const float4 m4 = me[j4];
           const float p0 = ex2(x[4 * j4] - m4.x), p1 = ex2(x[4 * j4 + 1] - m4.y);
           const float p2 = ex2(x[4 * j4 + 2] - m4.z), p3 = ex2(x[4 * j4 + 3] - m4.w);
-          lsum[4 * j4] += p0;
-          lsum[4 * j4 + 1] += p1;
-          lsum[4 * j4 + 2] += p2;
-          lsum[4 * j4 + 3] += p3;
+          lsum[4 * j4] += p0 * pf;
+          lsum[4 * j4 + 1] += p1 * pf;
+          lsum[4 * j4 + 2] += p2 * pf;
+          lsum[4 * j4 + 3] += p3 * pf;
           pk[2 * j4] = f32x2_f16x2(p0, p1);
           pk[2 * j4 + 1] = f32x2_f16x2(p2, p3);
         }
@@ -594,9 +655,9 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 
   if (n_split == 1) {
     if (tid < kHeads) sm.fac[tid] = sm.l_run[tid] > 0.f ? 1.f / sm.l_run[tid] : 0.f;
-    if (a.lse && tid < a.Hq) {
+    if (a.lse && hb + tid < a.Hq) {
       const float l = sm.l_run[tid];
-      a.lse[row * a.Hq + tid] = l > 0.f ? (sm.m_ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      a.lse[row * a.Hq + hb + tid] = l > 0.f ? (sm.m_ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
     if (!mma_warp) {
@@ -609,7 +670,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int h = c + j;
-          if (h < a.Hq) a.O[(row * a.Hq + h) * kD + 128 * mt + 32 * q4 + lane] = have_o ? o[j] * sm.fac[h] : 0.f;
+          if (hb + h < a.Hq) a.O[(row * a.Hq + hb + h) * kD + 128 * mt + 32 * q4 + lane] = have_o ? o[j] * sm.fac[h] : 0.f;
         }
       }
     }
@@ -620,23 +681,23 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     if (tid < kHeads) {
       // every rank's (m, l) of this head; the loads are independent (unrolled, predicated)
       const uint32_t am = tc::smem_addr(&sm.m_ref[tid]), al = tc::smem_addr(&sm.l_run[tid]);
-      float mq[kMaxChunks], lq[kMaxChunks];
+      float mq[kMaxSplit], lq[kMaxSplit];
 #pragma unroll
-      for (int q = 0; q < kMaxChunks; ++q) {
+      for (int q = 0; q < kMaxSplit; ++q) {
         mq[q] = q < n_split ? ld_cluster(map_to_rank(am, q)) : -INFINITY;
         lq[q] = q < n_split ? ld_cluster(map_to_rank(al, q)) : 0.f;
       }
       float M = -INFINITY;
 #pragma unroll
-      for (int q = 0; q < kMaxChunks; ++q) M = fmaxf(M, mq[q]);
+      for (int q = 0; q < kMaxSplit; ++q) M = fmaxf(M, mq[q]);
       float L = 0.f;
 #pragma unroll
-      for (int q = 0; q < kMaxChunks; ++q)
+      for (int q = 0; q < kMaxSplit; ++q)
         if (mq[q] != -INFINITY) L += lq[q] * ex2(mq[q] - M);
       const float mo = sm.m_ref[tid];
       sm.fac[tid] = (mo == -INFINITY || L <= 0.f) ? 0.f : ex2(mo - M) / L;
-      if (crank == 0 && a.lse && tid < a.Hq)
-        a.lse[row * a.Hq + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+      if (crank == 0 && a.lse && hb + tid < a.Hq)
+        a.lse[row * a.Hq + hb + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
     float* part = reinterpret_cast<float*>(sm.k);   // every MMA that read the K tile is complete
@@ -658,17 +719,17 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     const int h0 = kHeads * (int)crank / n_split, h1 = kHeads * ((int)crank + 1) / n_split;
     const uint32_t pbase = tc::smem_addr(part);
     for (int e = h0 * (kD / 4) + tid; e < h1 * (kD / 4); e += kThreads) {
-      float4 r[kMaxChunks];
+      float4 r[kMaxSplit];
 #pragma unroll
-      for (int q = 0; q < kMaxChunks; ++q)
+      for (int q = 0; q < kMaxSplit; ++q)
         r[q] = q < n_split ? ld_cluster4(map_to_rank(pbase + e * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
       float4 s4 = r[0];
 #pragma unroll
-      for (int q = 1; q < kMaxChunks; ++q) {
+      for (int q = 1; q < kMaxSplit; ++q) {
         s4.x += r[q].x; s4.y += r[q].y; s4.z += r[q].z; s4.w += r[q].w;
       }
       const int h = e / (kD / 4);
-      if (h < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + h) * kD + (e % (kD / 4)) * 4) = s4;
+      if (hb + h < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = s4;
     }
     cluster_sync();   // no CTA leaves while another still reads its shared memory
   }
@@ -681,7 +742,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 }  // namespace
 
 bool sparse_attn_tc_supported(const AttnArgs& a) {
-  return a.d == kD && a.Hq >= 1 && a.Hq <= kHeads && a.K >= 0 && a.W >= 0 &&
+  return a.d == kD && a.Hq >= 1 && a.Hq <= 2 * kHeads && a.K >= 0 && a.W >= 0 &&
          (int64_t)a.K + a.W <= (int64_t)kMaxChunks * kChunk && a.n_pages * kPage < ((int64_t)1 << 31) &&
          (int64_t)a.B * a.swa_cap < ((int64_t)1 << 31) - 2;
 }
@@ -695,13 +756,14 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int max_chunks = (int)((a.K + a.W + kChunk - 1) / kChunk);
   int n_split = 1;
-  if (rows < sms && max_chunks > 1) n_split = (int)std::max<int64_t>(1, std::min<int64_t>(max_chunks, sms / rows));
+  if (rows < sms && max_chunks > 1)
+    n_split = (int)std::max<int64_t>(1, std::min<int64_t>(std::min(max_chunks, kMaxSplit), sms / rows));
   const size_t smem = sizeof(TcSmem);
   e = cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (rows * n_split >= ((int64_t)1 << 31)) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(rows * n_split));
+  cfg.gridDim = dim3((unsigned)(rows * n_split), (unsigned)((a.Hq + kHeads - 1) / kHeads));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;

@@ -66,6 +66,30 @@ __device__ __forceinline__ uint32_t f32_to_bf16_bits(float f) {
 }
 
 // ---------------------------------------------------------------------------
+// fp16 attention operands (reading R11): powers of two that bring bf16 values
+// into fp16's range without touching a significand bit
+
+// 2^e as an fp32 value (e in [-126, 127]).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// Exponent f of a window row's dequantisation scale s: 0 while the row's
+// values bf16(e4m3 * s) are exact in fp16 (s in [2^-8, 2^7]: magnitudes in
+// [2^-17, 65504], every bf16 bit above 2^-24), else floor(log2 s) clamped to
+// [-100, 100]; the row is then dequantised with s * 2^-f (in [1, 2)), its
+// logits are multiplied by 2^f and its softmax weight p is carried as 2^f p.
+__device__ __forceinline__ int window_exp(float s) {
+  if (!(s > 0.f) || (s >= 0.00390625f && s <= 128.f)) return 0;
+  const int e = (int)((__float_as_uint(s) >> 23) & 0xFFu) - 127;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
+// Exponent e_h that scales a head of Q (largest bf16 exponent field eb, 0 for
+// an all-zero head) so that its largest magnitude lies in [2^14, 2^15).
+__device__ __forceinline__ int q_head_exp(int eb) {
+  return eb ? (eb - 141 < -110 ? -110 : (eb - 141 > 110 ? 110 : eb - 141)) : 0;
+}
+
+// ---------------------------------------------------------------------------
 // MXFP4 group of 16 channels (scale = E4M3(amax / 6), codes = E2M1(x / scale))
 
 struct Mxfp4Group {

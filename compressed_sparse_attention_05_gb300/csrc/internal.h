@@ -21,6 +21,11 @@ int report_error(int code, const char* msg);
 // Device status word of the current device (see csa2_get_status).
 uint32_t* status_word();
 
+// Device address of a module global in the calling thread's current context,
+// looked up with cudaGetSymbolAddress once per (context, symbol) and cached.
+// A context re-created by cudaDeviceReset gets a new id, hence a new lookup.
+void* symbol_address_cached(const void* symbol, cudaError_t* err);
+
 // Counts one kernel launch (csa2_launch_count) and returns the launch status.
 cudaError_t counted(cudaError_t launch_status);
 
@@ -182,7 +187,7 @@ struct AttnArgs {
   float* lse;                 // [rows][Hq] or null
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s);
-// ---- attention_tc.cu: tcgen05 kernel for d = 512, Hq <= 64, K + W <= 1024
+// ---- attention_tc.cu: tcgen05 kernel for d = 512 (every Hq and K + W the ABI admits)
 bool sparse_attn_tc_supported(const AttnArgs& a);
 cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s);
 

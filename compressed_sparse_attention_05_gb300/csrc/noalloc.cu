@@ -10,8 +10,6 @@
 // exits; every call shares it.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "internal.h"
 
@@ -21,24 +19,6 @@ namespace csa2 {
 constexpr size_t kNoAllocScratchBytes = 8u << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-
-// Device address of the array for the current device, looked up once per
-// device (with that device current) and cached.  Returns nullptr on failure.
-static void* noalloc_scratch_address(cudaError_t* err) {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    addr[dev] = p;
-  }
-  return addr[dev];
-}
 
 }  // namespace csa2
 
@@ -58,9 +38,13 @@ extern "C" int csa2_index_topk_noalloc(const csa2_dims* dims, const csa2_cache* 
                         "csa2_index_topk_noalloc: this shape needs more scratch than the fixed 8 MiB "
                         "device array (check csa2_index_topk_workspace_size); use csa2_index_topk with "
                         "a caller-allocated workspace instead");
+  // device address of the array in the current context (looked up once per context,
+  // with that context current, then cached; see symbol_address_cached)
   cudaError_t e = cudaSuccess;
-  void* scratch = noalloc_scratch_address(&e);
-  if (!scratch) return report_error(CSA2_ERR_CUDA, "csa2_index_topk_noalloc: cudaGetSymbolAddress failed");
+  void* scratch = symbol_address_cached(reinterpret_cast<const void*>(&g_noalloc_scratch), &e);
+  if (!scratch)
+    return report_error(CSA2_ERR_CUDA, e != cudaSuccess ? cudaGetErrorString(e)
+                                                        : "csa2_index_topk_noalloc: no device address for the scratch");
   // the histogram part of the scratch is cleared by the call itself; the rest
   // is written before it is read
   return index_topk_into(dims, cache, idx_q, w, q_pos, pool, pool_cnt, out_idx, out_cnt, out_pool,

@@ -28,7 +28,7 @@
  * Shapes (names follow the pages):
  *   B   sequences;  Tq query tokens per sequence (1 for decode)
  *   d   latent width (64 or 512); r rotated channels at its end (even, <= d)
- *   Hq  attention query heads (4 .. 64, multiple of 4; 64 in the pages' model)
+ *   Hq  attention query heads (1 .. 128; 64 in the pages' model)
  *   Hi, Di  indexer heads and head width (Hi <= 16, Di in {32, 64, 128})
  *   K   Top-K (1 .. 2048; 512 in the pages' model)
  *   W   sliding-window length in raw tokens (1 .. 1024; 128 in the pages)
@@ -79,6 +79,15 @@
  *      max(0, t-W+1) .. t that the window buffer holds}, logits
  *      q . k * softmax_scale (1/sqrt(d) in the pages' model), no sink; a
  *      key in both sets counts twice.  O is fp32, lse (natural log) optional.
+ *      Operand range: the products run on fp16 tensor-core operands with fp32
+ *      accumulation.  Every bf16 value keeps all its bits there: each head of
+ *      Q is scaled by a power of two that puts its largest magnitude in
+ *      [2^14, 2^15) (values below 2^-31 of that largest one lose bits), and a
+ *      window row whose scale lies outside [2^-8, 2^7] is dequantised with
+ *      the scale times 2^-f (f = floor(log2 scale), clamped to [-100, 100]),
+ *      its logits and softmax weights corrected by the same power.  MXFP4
+ *      values (<= 2688 in magnitude, >= 2^-10) need none.  Logits must stay
+ *      finite in fp32.
  *   R12 the indexer key of a new entry (Full layer with compression) is
  *      W_idx * [h_4j; ..; h_4j+3], rounded to the indexer dtype.
  *   R13 SWA Bounded Replay (csa2_swa_replay): a rebuilt window row is the
@@ -308,9 +317,11 @@ int csa2_index_topk(const csa2_dims* dims, const csa2_cache* cache, const void* 
  * (csa2_index_topk_noalloc_capacity() bytes), held by every GPU that loads
  * the library until the process exits.  Shapes whose
  * csa2_index_topk_workspace_size() exceeds it are rejected with
- * CSA2_ERR_WORKSPACE.  The first call on a device looks the array's device
- * address up (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  The call clears the part of the array that
+ * CSA2_ERR_WORKSPACE.  The first call in a CUDA context looks the array's
+ * device address up (cudaGetSymbolAddress) with that context current and
+ * caches it for that context; a context re-created by cudaDeviceReset is
+ * looked up again.  Make the first call in a context before any stream
+ * capture.  The call clears the part of the array that
  * must start at zero.  All calls share the one array: calls that can overlap
  * on the GPU (different streams without ordering between them) race and give
  * wrong results; order them on one stream.  Allocates nothing. */

@@ -4,8 +4,6 @@ Small workloads (several tiles, ragged tails) are checked on many query
 tokens; the full-size workloads, in the launch configuration the bench times,
 on sampled tokens.
 """
-import math
-
 import numpy as np
 import pytest
 import torch
@@ -13,7 +11,7 @@ import torch
 import parity
 from compressed_sparse_attention_05_gb300 import abi, build, harness
 from csa2_inputs import workloads as WL
-from oracle import attention as A
+from layer_check import _np, check_compressed_entries, check_group
 from oracle import indexer as I
 from oracle import layer as OL
 
@@ -24,64 +22,6 @@ pytestmark = pytest.mark.gpu
 def _lib():
     build.build()
     abi.lib()
-
-
-def _np(t):
-    return t.detach().cpu().double().numpy()
-
-
-def check_group(wl, samples, group=None):
-    """Run the layer group on the GPU and compare sampled tokens with the oracle."""
-    g = group or harness.LayerGroup(wl)
-    g.step()
-    torch.cuda.synchronize()
-    assert abi.csa2_get_status() == 0
-    tau = 1.0 / math.sqrt(wl.d)
-    qpos = wl.q_pos()
-    swaps = 0
-    states = {}
-    for (b, i) in samples:
-        st = states.setdefault(b, OL.SequenceState(wl, b))
-        t = int(qpos[b, i])
-        Kall = st.indexer_keys()
-        nv = I.n_visible(Kall.shape[0], t)
-        prev = None
-        pool = None
-        for l, mode in enumerate(wl.layers):
-            gi = g.idx[l][b, i].cpu().numpy()
-            gc = int(g.cnt[l][b, i])
-            if mode == "F":
-                q, w = _np(wl.idx_q_row(l, b, i)), _np(wl.idx_w_row(l, b, i))
-                s = I.index_scores(q, w, Kall[:nv])
-                cond = I.score_condition(q, w, Kall[:nv])
-                swaps += parity.check_topk_set(gi, gc, I.topk(s, wl.K), s, cond)
-                if wl.hierarchical:
-                    gp = g.pool[b, i].cpu().numpy()
-                    gpc = int(g.pool_cnt[b, i])
-                    bs = I.block_scores(s, 8)
-                    bcond = np.array([cond[8 * k:8 * k + 8].max() for k in range(len(bs))])
-                    swaps += parity.check_topk_set(gp, gpc, I.topk(bs, wl.pool_blocks), bs, bcond)
-                    pool = gp[:gpc]
-            elif mode == "X":
-                q, w = _np(wl.idx_q_row(l, b, i)), _np(wl.idx_w_row(l, b, i))
-                pos = I.pool_positions(pool, nv, 8)
-                s = I.index_scores(q, w, Kall[pos])
-                cond = I.score_condition(q, w, Kall[pos])
-                ref = pos[I.topk(s, wl.K)]
-                swaps += parity.check_topk_set(gi, gc, ref, s, cond, positions=pos)
-            else:
-                assert gc == prev[1] and np.array_equal(gi, prev[0])
-            assert np.all(4 * gi[:gc] + 3 <= t), "causality"
-            prev = (gi, gc)
-            # attention with the GPU's (verified) selection
-            Q = _np(wl.q_row(l, b, i))
-            O, lse = A.sparse_attention(Q, st.kv_rows(gi[:gc]), st.swa_rows(l, OL.window_of(wl, b, t)), tau)
-            err = parity.attn_err(g.O[l][b, i].cpu().numpy(), O)
-            assert err <= parity.ATTN_RTOL, f"layer {l} ({mode}) token {(b, i)}: attention error {err}"
-            # lse = log of the softmax normaliser; the kernels sum it from the fp32 or
-            # the fp16-rounded weights (relative difference <= 2^-11 per weight)
-            assert np.allclose(g.lse[l][b, i].cpu().numpy(), lse, rtol=0, atol=parity.LSE_ATOL)
-    return g, swaps
 
 
 def _decode_small():
@@ -104,18 +44,7 @@ def test_decode_small():
 def test_prefill_small_with_compression():
     wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
     g, _ = check_group(wl, [(0, i) for i in (0, 1, 2, 3, 4, 100, 254, 255)])
-    # the new entries were packed by the fused compression epilogue: compare bytes
-    st = OL.SequenceState(wl, 0)
-    new = st.new_entries()
-    ids = torch.from_numpy(new["entry_ids"])
-    slots = g.page_table[0, ids // 64].long().cpu() * 64 + ids % 64
-    codes = g.kv_codes[slots.cuda()].cpu().numpy()
-    scales = g.kv_scales[slots.cuda()].cpu().numpy()
-    # scales decided from the GEMM output: equal except at rounding boundaries
-    assert (scales != new["scales"]).mean() < 0.01
-    assert (codes != new["codes"]).mean() < 0.01
-    kk = g.idx_k[slots.cuda()].float().cpu().double().numpy()
-    assert np.allclose(kk, new["idx_k"], rtol=2e-2, atol=2e-2)
+    check_compressed_entries(g, wl, 0)
 
 
 def test_prefill_batch2_with_compression():
@@ -126,17 +55,8 @@ def test_prefill_batch2_with_compression():
                      description="2 sequences x 602 new tokens, hidden 256")
     g, _ = check_group(wl, [(0, 0), (0, 301), (0, 601), (1, 0), (1, 599), (1, 601)])
     for b in range(2):
-        st = OL.SequenceState(wl, b)
-        new = st.new_entries()
-        assert len(new["entry_ids"]) == 150
-        ids = torch.from_numpy(new["entry_ids"])
-        slots = g.page_table[b, ids // 64].long().cpu() * 64 + ids % 64
-        codes = g.kv_codes[slots.cuda()].cpu().numpy()
-        scales = g.kv_scales[slots.cuda()].cpu().numpy()
-        assert (scales != new["scales"]).mean() < 0.01
-        assert (codes != new["codes"]).mean() < 0.01
-        kk = g.idx_k[slots.cuda()].float().cpu().double().numpy()
-        assert np.allclose(kk, new["idx_k"], rtol=2e-2, atol=2e-2)
+        assert len(OL.SequenceState(wl, b).new_entries()["entry_ids"]) == 150
+        check_compressed_entries(g, wl, b)
 
 
 def test_encoder_stack_small():
@@ -250,5 +170,11 @@ def test_full_ragged_b64():
 
 
 def test_full_prefill_64k():
+    """The 4,096-token chunk as the bench times it: every one of the 1,024 new
+    entries (the 4H = 16,384 split-K compression GEMM over the [B][G][4H] tensor
+    map) byte-checked, and 64 query tokens spread over all 128 blocks of 32
+    tokens of the indexer GEMM and every lane position within a block."""
     wl = WL.prefill_64k()
-    check_group(wl, [(0, 0), (0, 2047), (0, 4095)])
+    toks = sorted({0, wl.Tq - 1} | {32 * (2 * k + (k & 1)) + (5 * k) % 32 for k in range(63)})
+    g, _ = check_group(wl, [(0, i) for i in toks])
+    check_compressed_entries(g, wl, 0)
