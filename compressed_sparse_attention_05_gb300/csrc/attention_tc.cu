@@ -32,9 +32,11 @@
 // chunks need no maximum reduction at all; row sums stay per thread until
 // the end of the token.
 //
-// Few tokens (decode): the chunks of a token are spread over a cluster of
-// up to 8 CTAs; each CTA finishes a partial (m, l, O) and the cluster merges
-// them through distributed shared memory, without global scratch.
+// Few tokens (decode): a token's keys are spread evenly over a cluster of up
+// to 8 CTAs; each CTA finishes a partial (m, l, O) and the cluster merges
+// them through distributed shared memory, without global scratch: every rank
+// owns a slice of the heads and sums the ranks' scaled partials of those heads
+// in rank order.
 //
 // Operands are fp16.  MXFP4 values (<= 6 significant bits, in [2^-10, 2688])
 // are exact.  bf16 values outside fp16's range are brought into it by powers
@@ -276,12 +278,18 @@ __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& k
   }
 }
 
-// Resolves key kk of the token's list: selected entry -> page table -> slot,
-// window position -> window row, else -1.
-__device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, int b, int kk, int n_sel, int n_keys,
-                                              int nv, int w_lo, int pos0, bool report, uint32_t* status) {
-  if (kk < n_sel) {
+// Resolves key kk of the token's list -- sel_cap selection slots (the first
+// n_sel of them selected entries), then window rows from raw position w_first --
+// to a main-KV slot (page table) or a window row, or -1 past the CTA's keys
+// [.., kk_end) or in an unused selection slot.  The index load does not wait for
+// n_sel when sel_cap is fixed (the cluster path lists all K slots).
+__device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, int b, int kk, int n_sel, int sel_cap,
+                                              int kk_end, int nv, int w_first, int pos0, bool report,
+                                              uint32_t* status) {
+  if (kk >= kk_end) return -1;
+  if (kk < sel_cap) {
     const int j = __ldg(a.idx + row * a.K + kk);
+    if (kk >= n_sel) return -1;
     if (j < 0 || j >= nv || (j >> 6) >= a.max_pages) {
       if (report) raise_status(status, CSA2_STATUS_BAD_INDEX);
       return -1;
@@ -293,8 +301,7 @@ __device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, in
     }
     return p * kPage + (j & (kPage - 1));
   }
-  if (kk < n_keys) return (int32_t)(-2 - ((int64_t)b * a.swa_cap + (w_lo + (kk - n_sel) - pos0)));
-  return -1;
+  return (int32_t)(-2 - ((int64_t)b * a.swa_cap + (w_first + (kk - sel_cap) - pos0)));
 }
 
 // Scores of the thread's key for heads 16*hg .. +15 in the log2 domain, as
@@ -333,6 +340,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   if (!ok) *abort = 1;
   return ok;
 }
+
+
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
@@ -423,6 +432,10 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
           make_uint4(ov[0], ov[1], ov[2], ov[3]);
     }
   }
+  // the window rows of the token: raw positions max(0, t-W+1, pos0) .. min(t, last row held)
+  const int w_lo = max(max(0, t - a.W + 1), pos0);
+  const int w_hi = min(t, pos0 + a.swa_cap - 1);
+  const int n_win = max(0, w_hi - w_lo + 1);
   // ---- the selection (and the window rows) come from earlier kernels of the step
   pdl_wait();
   int n_sel = a.cnt[row];
@@ -431,27 +444,27 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     if (tid == 0 && rank == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
     n_sel = n_sel < 0 ? 0 : a.K;
   }
-  // the key list: selected entries, then window rows
-  const int w_lo = max(max(0, t - a.W + 1), pos0);
-  const int w_hi = min(t, pos0 + a.swa_cap - 1);
-  const int n_win = max(0, w_hi - w_lo + 1);
-  const int n_keys = n_sel + n_win;
-  const int n_chunks = (n_keys + kChunk - 1) / kChunk;   // <= kMaxChunks (checked by the launcher)
-  const int c0 = n_chunks * rank / n_split, c1 = n_chunks * (rank + 1) / n_split;
-  const int n_my = c1 - c0;
+  // the key list: selection slots, then window rows.  One CTA per token lists the
+  // n_sel selected entries only; a cluster lists all K slots (unused ones empty),
+  // so that its ranks split the list without waiting for the count.
+  const int sel_cap = n_split > 1 ? a.K : n_sel;
+  const int n_keys = sel_cap + n_win;
+  // this CTA's keys: [kb0, kb1) of the list (balanced over the cluster)
+  const int kb0 = (int)((int64_t)n_keys * rank / n_split), kb1 = (int)((int64_t)n_keys * (rank + 1) / n_split);
+  const int n_my = (kb1 - kb0 + kChunk - 1) / kChunk;   // chunks of kChunk keys, <= kMaxChunks
 
   // ---- key sources.  Every worker resolves its key in the first chunk; the
   // key's later chunks are shared out among its four threads.
   int32_t cur_src = -1;
   if (!mma_warp && n_my > 0) {
-    cur_src = key_source(a, row, b, c0 * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, qd == 0, status);
+    cur_src = key_source(a, row, b, kb0 + key, n_sel, sel_cap, kb1, nv, w_lo, pos0, qd == 0, status);
     if (qd == 0) {
       sm.slot[key] = cur_src;
       sm.kexp[key] = (int8_t)(cur_src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)cur_src))) : 0);
     }
     for (int c = qd + 1; c < n_my; c += 4) {
       const int32_t src =
-          key_source(a, row, b, (c0 + c) * kChunk + key, n_sel, n_keys, nv, w_lo, pos0, true, status);
+          key_source(a, row, b, kb0 + c * kChunk + key, n_sel, sel_cap, kb1, nv, w_lo, pos0, true, status);
       sm.slot[c * kChunk + key] = src;
       sm.kexp[c * kChunk + key] = (int8_t)(src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)src))) : 0);
     }
@@ -498,10 +511,11 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
         tc::mma_commit(&sm.bar_s);
         if (!tc::mbar_wait(&sm.p_ready, it & 1, 1u << 22)) { *abort = 1; break; }
         tc::tc_fence_after();
+        // PV over the chunk's keys only (a short last chunk skips its empty 16-key steps)
+        const int ksteps = (min(kChunk, kb1 - kb0 - kChunk * it) + 15) / 16;
 #pragma unroll
         for (int mt = 0; mt < 4; ++mt) {   // tile by tile: a finished tile frees its K slice for the next chunk
-#pragma unroll
-          for (int kk = 0; kk < kChunk / 16; ++kk)
+          for (int kk = 0; kk < ksteps; ++kk)
             tc::mma_f16(tm + kColO + 64 * mt, dk_o + (uint64_t)(mt * 128 + kk * 1024), dp_o + (uint64_t)(kk * 128),
                         kIdO, (it > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(&sm.bar_pv[mt]);
@@ -675,7 +689,11 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       }
     }
   } else {
-    // ---- merge the cluster's partials: (m, l) first, then the scaled O
+    // ---- merge the cluster's partials: (m, l) first, then the scaled O.  Every
+    // rank writes its scaled partial O to its own shared memory; rank r then sums
+    // heads [own(r), own(r+1)) over the ranks in rank order, every remote value
+    // requested before any is added (the reads are latency-bound: all of a
+    // thread's loads are in flight together).
     const uint32_t crank = cluster_rank();
     cluster_sync();
     if (tid < kHeads) {
@@ -714,22 +732,58 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       }
     }
     cluster_sync();
-    // this rank sums heads h0 .. h1 over all ranks, every rank's value
-    // requested before any is added
     const int h0 = kHeads * (int)crank / n_split, h1 = kHeads * ((int)crank + 1) / n_split;
     const uint32_t pbase = tc::smem_addr(part);
-    for (int e = h0 * (kD / 4) + tid; e < h1 * (kD / 4); e += kThreads) {
-      float4 r[kMaxSplit];
+    const int n4 = (h1 - h0) * (kD / 4);   // float4 elements of this rank's heads (<= 13 heads: 3,328)
+    constexpr int kPer = (kHeads / 5 + 1) * (kD / 4) / kThreads + 1;   // per thread, for n_split >= 5
+    if (n_split >= 5) {
+      float4 acc[kPer];
 #pragma unroll
-      for (int q = 0; q < kMaxSplit; ++q)
-        r[q] = q < n_split ? ld_cluster4(map_to_rank(pbase + e * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 s4 = r[0];
+      for (int u = 0; u < kPer; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q = 0; q < n_split; ++q) {   // rank order; a rank's loads are all issued before they are added
+        float4 r[kPer];
 #pragma unroll
-      for (int q = 1; q < kMaxSplit; ++q) {
-        s4.x += r[q].x; s4.y += r[q].y; s4.z += r[q].z; s4.w += r[q].w;
+        for (int u = 0; u < kPer; ++u) {
+          const int e = tid + u * kThreads;
+          r[u] = e < n4 ? ld_cluster4(map_to_rank(pbase + (h0 * (kD / 4) + e) * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {
+          acc[u].x += r[u].x; acc[u].y += r[u].y; acc[u].z += r[u].z; acc[u].w += r[u].w;
+        }
       }
-      const int h = e / (kD / 4);
-      if (hb + h < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = s4;
+#pragma unroll
+      for (int u = 0; u < kPer; ++u) {
+        const int e = tid + u * kThreads;
+        const int h = h0 + e / (kD / 4);
+        if (e < n4 && hb + h < a.Hq)
+          *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = acc[u];
+      }
+    } else {
+      // up to 4 ranks (16 or more heads each): four elements x every rank's value in flight
+      for (int e0 = tid; e0 < n4; e0 += 4 * kThreads) {
+        float4 r[4][4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * kThreads;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            r[u][q] = (q < n_split && e < n4) ? ld_cluster4(map_to_rank(pbase + (h0 * (kD / 4) + e) * 16, q))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = e0 + u * kThreads;
+          float4 s4 = r[u][0];
+#pragma unroll
+          for (int q = 1; q < 4; ++q) {
+            s4.x += r[u][q].x; s4.y += r[u][q].y; s4.z += r[u][q].z; s4.w += r[u][q].w;
+          }
+          const int h = h0 + e / (kD / 4);
+          if (e < n4 && hb + h < a.Hq)
+            *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = s4;
+        }
+      }
     }
     cluster_sync();   // no CTA leaves while another still reads its shared memory
   }

@@ -41,6 +41,14 @@ def test_decode_small():
     check_group(wl, [(0, 0), (1, 0), (2, 0)])
 
 
+def test_decode_small_k1024():
+    """Top-1024: nine 128-key chunks per token spread over a cluster of six CTAs
+    (uneven head slices in the merge), a short last chunk on every rank."""
+    wl = _decode_small()
+    wl.K = 1024
+    check_group(wl, [(0, 0), (1, 0), (2, 0)])
+
+
 def test_prefill_small_with_compression():
     wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
     g, _ = check_group(wl, [(0, i) for i in (0, 1, 2, 3, 4, 100, 254, 255)])
