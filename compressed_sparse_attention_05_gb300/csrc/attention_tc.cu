@@ -278,18 +278,18 @@ __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& k
   }
 }
 
-// Resolves key kk of the token's list -- sel_cap selection slots (the first
-// n_sel of them selected entries), then window rows from raw position w_first --
-// to a main-KV slot (page table) or a window row, or -1 past the CTA's keys
-// [.., kk_end) or in an unused selection slot.  The index load does not wait for
-// n_sel when sel_cap is fixed (the cluster path lists all K slots).
-__device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, int b, int kk, int n_sel, int sel_cap,
-                                              int kk_end, int nv, int w_first, int pos0, bool report,
+// Resolves key kk of a CTA's key list -- sel_cap selection slots (slots sel_off ..
+// of the token's Top-K, the first n_sel of which hold selected entries), then
+// window rows from raw position w_first -- to a main-KV slot (page table) or a
+// window row, or -1 past the list [.., kk_end) or in an unused selection slot.
+// The index load does not wait for n_sel when sel_cap is fixed (the cluster path).
+__device__ __forceinline__ int32_t key_source(const AttnArgs& a, int64_t row, int b, int kk, int n_sel, int sel_off,
+                                              int sel_cap, int kk_end, int nv, int w_first, int pos0, bool report,
                                               uint32_t* status) {
   if (kk >= kk_end) return -1;
   if (kk < sel_cap) {
-    const int j = __ldg(a.idx + row * a.K + kk);
-    if (kk >= n_sel) return -1;
+    const int j = __ldg(a.idx + row * a.K + sel_off + kk);
+    if (sel_off + kk >= n_sel) return -1;
     if (j < 0 || j >= nv || (j >> 6) >= a.max_pages) {
       if (report) raise_status(status, CSA2_STATUS_BAD_INDEX);
       return -1;
@@ -444,27 +444,34 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     if (tid == 0 && rank == 0) raise_status(status, CSA2_STATUS_BAD_COUNT);
     n_sel = n_sel < 0 ? 0 : a.K;
   }
-  // the key list: selection slots, then window rows.  One CTA per token lists the
-  // n_sel selected entries only; a cluster lists all K slots (unused ones empty),
-  // so that its ranks split the list without waiting for the count.
-  const int sel_cap = n_split > 1 ? a.K : n_sel;
-  const int n_keys = sel_cap + n_win;
-  // this CTA's keys: [kb0, kb1) of the list (balanced over the cluster)
-  const int kb0 = (int)((int64_t)n_keys * rank / n_split), kb1 = (int)((int64_t)n_keys * (rank + 1) / n_split);
+  // the key list.  One CTA per token: its n_sel selected entries, then its window
+  // rows.  A cluster: rank r takes an equal share of the K selection slots (unused
+  // ones empty, so that the index loads need not wait for the count) and an equal
+  // share of the window rows.
+  int sel_off = 0, sel_cap = n_sel, w_first = w_lo, n_mine = n_sel + n_win;
+  if (n_split > 1) {
+    sel_off = (int)((int64_t)a.K * rank / n_split);
+    sel_cap = (int)((int64_t)a.K * (rank + 1) / n_split) - sel_off;
+    const int u0 = (int)((int64_t)n_win * rank / n_split), u1 = (int)((int64_t)n_win * (rank + 1) / n_split);
+    w_first = w_lo + u0;
+    n_mine = sel_cap + (u1 - u0);
+  }
+  const int kb0 = 0, kb1 = n_mine;
   const int n_my = (kb1 - kb0 + kChunk - 1) / kChunk;   // chunks of kChunk keys, <= kMaxChunks
 
   // ---- key sources.  Every worker resolves its key in the first chunk; the
   // key's later chunks are shared out among its four threads.
   int32_t cur_src = -1;
   if (!mma_warp && n_my > 0) {
-    cur_src = key_source(a, row, b, kb0 + key, n_sel, sel_cap, kb1, nv, w_lo, pos0, qd == 0, status);
+    cur_src = key_source(a, row, b, kb0 + key, n_sel, sel_off, sel_cap, kb1, nv, w_first, pos0, qd == 0, status);
     if (qd == 0) {
       sm.slot[key] = cur_src;
       sm.kexp[key] = (int8_t)(cur_src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)cur_src))) : 0);
     }
     for (int c = qd + 1; c < n_my; c += 4) {
       const int32_t src =
-          key_source(a, row, b, kb0 + c * kChunk + key, n_sel, sel_cap, kb1, nv, w_lo, pos0, true, status);
+          key_source(a, row, b, kb0 + c * kChunk + key, n_sel, sel_off, sel_cap, kb1, nv, w_first, pos0, true,
+                     status);
       sm.slot[c * kChunk + key] = src;
       sm.kexp[c * kChunk + key] = (int8_t)(src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)src))) : 0);
     }
@@ -689,13 +696,28 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       }
     }
   } else {
-    // ---- merge the cluster's partials: (m, l) first, then the scaled O.  Every
-    // rank writes its scaled partial O to its own shared memory; rank r then sums
-    // heads [own(r), own(r+1)) over the ranks in rank order, every remote value
-    // requested before any is added (the reads are latency-bound: all of a
-    // thread's loads are in flight together).
-    const uint32_t crank = cluster_rank();
-    cluster_sync();
+    // ---- merge the cluster's partials with one exchange.  Every rank publishes its
+    // (m, l) and its unscaled partial O in its own shared memory, [head][dim] (a
+    // warp's remote reads below are then contiguous); after one cluster barrier
+    // rank r sums heads [own(r), own(r+1)) over the ranks in rank order, each rank's
+    // partial scaled by 2^(m_q - M) / L.
+    const int crank = (int)cluster_rank();
+    float* part = reinterpret_cast<float*>(sm.k);   // every MMA that read the K tile is complete
+    if (!mma_warp) {
+      const int dim = 128 * mt + 32 * q4 + lane;
+      for (int c = 0; c < kHeads; c += 16) {
+        float o[16];
+        if (have_o) {
+          tc::tmem_ld16(tm + kColO + 64 * mt + c + ((uint32_t)(32 * q4) << 16), o);
+          tc::tmem_wait_ld();
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(c + j) * kD + dim] = have_o ? o[j] : 0.f;
+      }
+    }
+    cluster_sync();   // every rank's (m, l) and partial O are published
+    const int h0 = kHeads * crank / n_split, h1 = kHeads * (crank + 1) / n_split;
+    float* facq = reinterpret_cast<float*>(sm.q);    // [rank][head]: the Q tile is no longer read
     if (tid < kHeads) {
       // every rank's (m, l) of this head; the loads are independent (unrolled, predicated)
       const uint32_t am = tc::smem_addr(&sm.m_ref[tid]), al = tc::smem_addr(&sm.l_run[tid]);
@@ -712,77 +734,39 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 #pragma unroll
       for (int q = 0; q < kMaxSplit; ++q)
         if (mq[q] != -INFINITY) L += lq[q] * ex2(mq[q] - M);
-      const float mo = sm.m_ref[tid];
-      sm.fac[tid] = (mo == -INFINITY || L <= 0.f) ? 0.f : ex2(mo - M) / L;
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q)
+        if (q < n_split) facq[q * kHeads + tid] = (mq[q] == -INFINITY || L <= 0.f) ? 0.f : ex2(mq[q] - M) / L;
       if (crank == 0 && a.lse && hb + tid < a.Hq)
         a.lse[row * a.Hq + hb + tid] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
     __syncthreads();
-    float* part = reinterpret_cast<float*>(sm.k);   // every MMA that read the K tile is complete
-    if (!mma_warp) {
-      for (int c = 0; c < kHeads; c += 16) {
-        float o[16];
-        if (have_o) {
-          tc::tmem_ld16(tm + kColO + 64 * mt + c + ((uint32_t)(32 * q4) << 16), o);
-          tc::tmem_wait_ld();
-        }
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          part[(c + j) * kD + 128 * mt + 32 * q4 + lane] = have_o ? o[j] * sm.fac[c + j] : 0.f;
-      }
-    }
-    cluster_sync();
-    const int h0 = kHeads * (int)crank / n_split, h1 = kHeads * ((int)crank + 1) / n_split;
+    // this rank's heads, 4 dims per element; every rank's value of two elements in flight
     const uint32_t pbase = tc::smem_addr(part);
-    const int n4 = (h1 - h0) * (kD / 4);   // float4 elements of this rank's heads (<= 13 heads: 3,328)
-    constexpr int kPer = (kHeads / 5 + 1) * (kD / 4) / kThreads + 1;   // per thread, for n_split >= 5
-    if (n_split >= 5) {
-      float4 acc[kPer];
+    const int n4 = (h1 - h0) * (kD / 4);
+    for (int e0 = tid; e0 < n4; e0 += 2 * kThreads) {
+      float4 r[2][kMaxSplit];
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q = 0; q < n_split; ++q) {   // rank order; a rank's loads are all issued before they are added
-        float4 r[kPer];
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + u * kThreads;
 #pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          const int e = tid + u * kThreads;
-          r[u] = e < n4 ? ld_cluster4(map_to_rank(pbase + (h0 * (kD / 4) + e) * 16, q)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < kPer; ++u) {
-          acc[u].x += r[u].x; acc[u].y += r[u].y; acc[u].z += r[u].z; acc[u].w += r[u].w;
-        }
+        for (int q = 0; q < kMaxSplit; ++q)
+          r[u][q] = (q < n_split && e < n4) ? ld_cluster4(map_to_rank(pbase + 16u * (uint32_t)(h0 * (kD / 4) + e), q))
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < kPer; ++u) {
-        const int e = tid + u * kThreads;
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + u * kThreads;
+        if (e >= n4) continue;
         const int h = h0 + e / (kD / 4);
-        if (e < n4 && hb + h < a.Hq)
-          *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = acc[u];
-      }
-    } else {
-      // up to 4 ranks (16 or more heads each): four elements x every rank's value in flight
-      for (int e0 = tid; e0 < n4; e0 += 4 * kThreads) {
-        float4 r[4][4];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * kThreads;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            r[u][q] = (q < n_split && e < n4) ? ld_cluster4(map_to_rank(pbase + (h0 * (kD / 4) + e) * 16, q))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < kMaxSplit; ++q) {
+          if (q >= n_split) break;
+          const float f = facq[q * kHeads + h];
+          acc.x += r[u][q].x * f; acc.y += r[u][q].y * f; acc.z += r[u][q].z * f; acc.w += r[u][q].w * f;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = e0 + u * kThreads;
-          float4 s4 = r[u][0];
-#pragma unroll
-          for (int q = 1; q < 4; ++q) {
-            s4.x += r[u][q].x; s4.y += r[u][q].y; s4.z += r[u][q].z; s4.w += r[u][q].w;
-          }
-          const int h = h0 + e / (kD / 4);
-          if (e < n4 && hb + h < a.Hq)
-            *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = s4;
-        }
+        if (hb + h < a.Hq) *reinterpret_cast<float4*>(a.O + (row * a.Hq + hb + h) * kD + (e % (kD / 4)) * 4) = acc;
       }
     }
     cluster_sync();   // no CTA leaves while another still reads its shared memory
