@@ -1,7 +1,7 @@
 """Benchmark of the CSA2 layer step on GB300 (prints one JSON line).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|hierarchical|ragged|
-                    encoder_stack|decoder_stack|decoder_stack_prefill|decoder_replay|ced_compress]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|decode_fp8kv|prefill|hierarchical|
+                    ragged|encoder_stack|decoder_stack|decoder_stack_prefill|decoder_replay|ced_compress]
     python bench.py --impl reference ...      # the CPU oracle on a bounded sample
 
 A step is one pass of the layer group over one batch of synthetic input,
@@ -38,19 +38,26 @@ FLUSH_BYTES = 512 << 20
 # ---------------------------------------------------------------------------------
 # workload bytes / flops (algorithmic: what the method must move or compute)
 
+def kv_desc(wl):
+    if getattr(wl, "kv_format", "mxfp4") == "fp8":
+        return f"FP8 E4M3 + fp32 scale, {wl.d + 4} B/entry, 64-entry pages"
+    return f"MXFP4 {wl.d // 2 + wl.d // 16} B/entry, 64-entry pages"
+
+
 def algorithmic(wl):
     """Per-step algorithmic work of the workload's hot path: unique HBM bytes and FLOPs.
 
     Bytes count what a step must move at least once: each sequence's visible
     indexer keys per Full layer (all query tokens of a sequence share them),
     the pooled keys per Reindex layer (the pools of one sequence's tokens overlap,
-    so at most its visible keys), the selected MXFP4 entries (at most the
+    so at most its visible keys), the selected MXFP4 (or FP8) entries (at most the
     entries that exist), the queries read, the outputs written and the index
     scores written and read back once, plus the hidden states of a prefill
     chunk.  For one query token per sequence this is the per-query sum.
     """
     d, Di, K, W, Hq = wl.d, wl.Di, wl.K, wl.W, wl.Hq
-    entry_bytes = d // 2 + d // 16                       # 288 B MXFP4 entry (d = 512)
+    fp8kv = getattr(wl, "kv_format", "mxfp4") == "fp8"
+    entry_bytes = d + 4 if fp8kv else d // 2 + d // 16    # 516 B FP8 / 288 B MXFP4 entry (d = 512)
     idx_elt = 2 if wl.idx_dtype == "bf16" else 4
     scan = 0          # indexer keys read by Full layers (unique per sequence)
     pooled = 0        # indexer keys read by Reindex layers
@@ -284,7 +291,7 @@ def measure(args, workload, steps, rank, world, dist, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": tokens,
                    "layers": "".join(wl.layers), "K": wl.K, "Hq": wl.Hq, "d": wl.d, "W": wl.W,
-                   "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": "MXFP4 288 B/entry, 64-entry pages",
+                   "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": kv_desc(wl),
                    "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
@@ -829,7 +836,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "hierarchical", "ragged", "encoder_stack", "decoder_stack",
+                    choices=["decode", "decode_fp8kv", "prefill", "hierarchical", "ragged", "encoder_stack",
+                             "decoder_stack",
                              "decoder_stack_prefill", "decoder_replay", "ced_compress"])
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

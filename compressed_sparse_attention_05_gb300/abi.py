@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libcsa2.so")
 
 CSA2_OK = 0
 CSA2_F32, CSA2_BF16 = 0, 1
+CSA2_KV_MXFP4, CSA2_KV_FP8 = 0, 1
 MODE_FULL, MODE_REINDEX, MODE_REUSE = 0, 1, 2
 STATUS_BAD_PAGE, STATUS_BAD_INDEX, STATUS_BAD_COUNT = 1, 2, 4
 
@@ -33,7 +34,7 @@ class Csa2Error(RuntimeError):
 
 class Dims(C.Structure):
     _fields_ = [(n, C.c_int32) for n in ("B", "Tq", "d", "r", "Hq", "Hi", "Di", "idx_dtype", "K", "W",
-                                        "max_pages", "n_pool_blocks", "pool_block", "swa_cap")]
+                                        "max_pages", "n_pool_blocks", "pool_block", "swa_cap", "kv_format")]
 
 
 class Cache(C.Structure):
@@ -72,6 +73,8 @@ SIGNATURES = {
     "csa2_pack_swa_fp8": (C.c_int, [_P, _I64, _I32, _P, _P, _P]),
     "csa2_norm_rope_pack": (C.c_int, [_P, _I32, _I32, _I32, _I32, _P, _F, _F, _P, _P, _P, _I32, _I64,
                                       _P, _P, _P]),
+    "csa2_norm_rope_pack_fp8": (C.c_int, [_P, _I32, _I32, _I32, _I32, _P, _F, _F, _P, _P, _P, _I32, _I64,
+                                          _P, _P, _P]),
     "csa2_compress_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "csa2_compress_pack": (C.c_int, [_P, _I32, _I32, _I32, _P, _P, _F, _F, _P, _P, C.POINTER(Dims),
                                      C.POINTER(Cache), _P, _SZ, _P]),
@@ -178,6 +181,14 @@ def csa2_norm_rope_pack(latent, r, gamma, eps, rope_base, first_entry, n_rows, p
     _check(lib().csa2_norm_rope_pack(ptr(latent), B, n_max, d, r, ptr(gamma), eps, rope_base,
                                      ptr(first_entry), ptr(n_rows), ptr(page_table), page_table.shape[1],
                                      n_pages, ptr(kv_codes), ptr(kv_scales), stream_handle(stream)))
+
+
+def csa2_norm_rope_pack_fp8(latent, r, gamma, eps, rope_base, first_entry, n_rows, page_table, n_pages,
+                            kv_codes, kv_scales, stream=None):
+    B, n_max, d = latent.shape
+    _check(lib().csa2_norm_rope_pack_fp8(ptr(latent), B, n_max, d, r, ptr(gamma), eps, rope_base,
+                                         ptr(first_entry), ptr(n_rows), ptr(page_table), page_table.shape[1],
+                                         n_pages, ptr(kv_codes), ptr(kv_scales), stream_handle(stream)))
 
 
 def csa2_compress_workspace_size(B, T, H, d, Di) -> int:

@@ -139,6 +139,9 @@ static int check_dims(const csa2_dims* dm, bool need_indexer, bool need_attn) {
     REQUIRE(dm->idx_dtype == CSA2_BF16 || dm->idx_dtype == CSA2_F32, "idx_dtype must be CSA2_BF16 or CSA2_F32");
     REQUIRE(dm->K >= 1 && dm->K <= 2048, "K must be in 1..2048 (got %d)", dm->K);
   }
+  REQUIRE(dm->kv_format == CSA2_KV_MXFP4 || dm->kv_format == CSA2_KV_FP8, "kv_format must be CSA2_KV_MXFP4 or CSA2_KV_FP8");
+  if (dm->kv_format == CSA2_KV_FP8 && dm->d != 512)
+    return fail(CSA2_ERR_UNSUPPORTED, "the FP8 main-KV format needs d = 512 (got %d)", dm->d);
   if (need_attn) {
     if (dm->d != 64 && dm->d != 512) return fail(CSA2_ERR_UNSUPPORTED, "d must be 64 or 512 (got %d)", dm->d);
     REQUIRE(dm->Hq >= 1 && dm->Hq <= 128, "Hq must be in 1..128 (got %d)", dm->Hq);
@@ -294,6 +297,28 @@ int csa2_norm_rope_pack(const float* latent, int32_t B, int32_t n_max, int32_t d
   return CSA2_OK;
 }
 
+int csa2_norm_rope_pack_fp8(const float* latent, int32_t B, int32_t n_max, int32_t d, int32_t r,
+                            const float* gamma, float eps, float rope_base, const int32_t* first_entry,
+                            const int32_t* n_rows, const int32_t* page_table, int32_t max_pages,
+                            int64_t n_pages, uint8_t* kv_codes, float* kv_scales, void* stream) {
+  NvtxRange nvtx_("csa2_norm_rope_pack_fp8");
+  g_err[0] = 0;
+  REQUIRE(B >= 0 && n_max >= 0, "B and n_max must be >= 0");
+  if (d != 512) return fail(CSA2_ERR_UNSUPPORTED, "the FP8 main-KV format needs d = 512 (got %d)", d);
+  REQUIRE(r >= 0 && r <= d && r % 2 == 0, "r must be even and in 0..d (got %d)", r);
+  REQUIRE(eps >= 0.f, "eps must be >= 0");
+  if ((int64_t)B * n_max == 0) return CSA2_OK;
+  REQUIRE_PTR(latent); REQUIRE_PTR(gamma); REQUIRE_IPTR(first_entry); REQUIRE_IPTR(n_rows);
+  REQUIRE_IPTR(page_table); REQUIRE_PTR(kv_codes); REQUIRE_PTR(kv_scales);
+  REQUIRE(max_pages >= 1 && n_pages >= 1, "max_pages and n_pages must be >= 1");
+  LatentSource src{latent, d, 0, 1};
+  LAUNCH(launch_norm_rope_pack(src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table,
+                               max_pages, n_pages, kv_codes, reinterpret_cast<uint8_t*>(kv_scales), nullptr, 0, 0, 0,
+                               nullptr, static_cast<cudaStream_t>(stream), 1),
+         "norm_rope_pack_fp8");
+  return CSA2_OK;
+}
+
 size_t csa2_compress_workspace_size(int32_t B, int32_t T, int32_t H, int32_t d, int32_t Di) {
   if (B <= 0 || T < 4 || H <= 0 || d <= 0) return 0;
   return compress_partials_bytes(B, T, H, d, Di > 0 ? Di : 0, nullptr);
@@ -345,7 +370,8 @@ int csa2_compress_pack(const uint16_t* hidden, int32_t B, int32_t T, int32_t H, 
   LatentSource src{part, N, (int64_t)B * G * N, n_split};
   LAUNCH(launch_norm_rope_pack(src, B, G, dm->d, dm->r, gamma, eps, rope_base, first_entry, nullptr,
                                c->page_table, dm->max_pages, c->n_pages, c->kv_codes, c->kv_scales,
-                               W_idx ? part + dm->d : nullptr, N, Di, dm->idx_dtype, W_idx ? c->idx_k : nullptr, s),
+                               W_idx ? part + dm->d : nullptr, N, Di, dm->idx_dtype, W_idx ? c->idx_k : nullptr, s,
+                               dm->kv_format == CSA2_KV_FP8),
          "compress_epilogue");
   return CSA2_OK;
 }
@@ -403,7 +429,7 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
     LAUNCH(launch_norm_rope_pack(src, B, G, d, dm->r, gamma_all + (int64_t)l * d, eps, rope_base, first_entry,
                                  nullptr, c->page_table, dm->max_pages, c->n_pages, c->kv_codes, c->kv_scales,
                                  Di ? part + (int64_t)l * Nl + d : nullptr, N, Di, dm->idx_dtype,
-                                 Di ? c->idx_k : nullptr, s),
+                                 Di ? c->idx_k : nullptr, s, dm->kv_format == CSA2_KV_FP8),
            "compress_layers_epilogue");
   }
   return CSA2_OK;
@@ -659,6 +685,7 @@ static int attn_impl(const csa2_dims* dm, const csa2_cache* c, const csa2_window
   a.n_entries = c->n_entries; a.swa_codes = win->codes; a.swa_scales = win->scales; a.swa_pos0 = win->pos0;
   a.swa_cap = (dm->W > 0) ? dm->swa_cap : 0; a.W = dm->W; a.B = dm->B; a.Tq = dm->Tq; a.Hq = dm->Hq;
   a.d = dm->d; a.K = dm->K; a.scale = softmax_scale; a.O = O; a.lse = lse;
+  a.kv_fp8 = dm->kv_format == CSA2_KV_FP8;
   LAUNCH(launch_sparse_attn(a, s), "sparse_attn");
   return CSA2_OK;
 }

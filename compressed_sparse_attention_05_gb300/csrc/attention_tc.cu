@@ -46,7 +46,11 @@
 // outside [2^-8, 2^7] is dequantised with the scale 2^-f s (s' in [1, 2)), its
 // logits multiplied back by 2^f and its softmax weight carried as 2^f p in the
 // PV product (the reference maximum then follows the largest 2^f p, and the
-// normaliser adds p itself).  P is rounded to fp16 for the PV product; the
+// normaliser adds p itself).  Main-KV entries in the FP8 format (the V4-style
+// layout kept for the A/B against MXFP4: E4M3 row + fp32 scale, one 32-byte
+// run of codes per thread and slice) go through the window rows' path: code x
+// scale rounded to bf16, the same power-of-two treatment; the kernel is
+// instantiated once per format.  P is rounded to fp16 for the PV product; the
 // normaliser sums the unrounded fp32 P (relative difference <= 2^-11).
 // Accumulation is fp32.
 #include <cuda_fp16.h>
@@ -227,24 +231,62 @@ __device__ __forceinline__ uint2 load_scales(const AttnArgs& a, int32_t src, int
                   : make_uint2(0, 0);
 }
 
-template <int SL>
+// Packed bytes of slice SL of a main-KV key for the thread's 32 dims.  MXFP4:
+// 16 bytes, in v[SL].  FP8 rows: 32 bytes, in v[2 (SL & 1)] and the next (slices
+// 0 and 1 are prefetched together, slices 2 and 3 reuse their registers).
+template <int SL, bool kFp8>
 __device__ __forceinline__ void load_slice(const AttnArgs& a, int32_t src, int qd, KeyBytes& kb) {
-  if (src >= 0)
+  if (src < 0) return;
+  if (kFp8) {
+    const uint8_t* p = a.kv_codes + (int64_t)src * kD + 32 * qd + 128 * SL;
+    kb.v[2 * (SL & 1)] = __ldg(reinterpret_cast<const uint4*>(p));
+    kb.v[2 * (SL & 1) + 1] = __ldg(reinterpret_cast<const uint4*>(p + 16));
+  } else {
     kb.v[SL] = __ldg(reinterpret_cast<const uint4*>(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL));
+  }
 }
-// Dequantisation scale of a window row, times 2^-f (see window_exp).
+// Dequantisation scale of an FP8 row (a window row, or a main-KV entry in the FP8
+// format), times 2^-f (see window_exp); 0 for an MXFP4 entry or no key.
+template <bool kFp8>
 __device__ __forceinline__ float load_wscale(const AttnArgs& a, int32_t src) {
-  if (src > -2) return 0.f;
-  const float sw = __ldg(a.swa_scales + (-2 - (int64_t)src));
+  float sw;
+  if (src <= -2) sw = __ldg(a.swa_scales + (-2 - (int64_t)src));
+  else if (kFp8 && src >= 0) sw = __ldg(reinterpret_cast<const float*>(a.kv_scales) + src);
+  else return 0.f;
   return sw * pow2i(-window_exp(sw));
+}
+// Exponent f of a key's FP8 scale (0 for MXFP4 entries and missing keys).
+template <bool kFp8>
+__device__ __forceinline__ int key_exp(const AttnArgs& a, int32_t src) {
+  if (src <= -2) return window_exp(__ldg(a.swa_scales + (-2 - (int64_t)src)));
+  if (kFp8 && src >= 0) return window_exp(__ldg(reinterpret_cast<const float*>(a.kv_scales) + src));
+  return 0;
+}
+
+// 32 E4M3 codes (c0: dims 0-15, c1: 16-31) times the (2^-f scaled) row scale,
+// rounded to bf16 as the operand rule says, into 4 core-matrix rows of fp16.
+__device__ __forceinline__ void store_fp8_dims(uint4 c0, uint4 c1, float sc, unsigned char* dst) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 c = j < 2 ? c0 : c1;
+    const uint32_t w0 = word_of(c, (j & 1) * 2), w1 = word_of(c, (j & 1) * 2 + 1);
+    uint4 o;
+    o.x = win2_f16x2(w0 & 0xFFFFu, sc);
+    o.y = win2_f16x2(w0 >> 16, sc);
+    o.z = win2_f16x2(w1 & 0xFFFFu, sc);
+    o.w = win2_f16x2(w1 >> 16, sc);
+    *reinterpret_cast<uint4*>(dst + j * 128) = o;
+  }
 }
 
 // Dequantise the thread's 32 dims of slice SL into the K tile (4 core-matrix rows).
-template <int SL>
+template <int SL, bool kFp8>
 __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& kb, uint32_t sc_pair, int32_t src,
                                             float wsc, int key, int qd, unsigned char* ktile) {
   unsigned char* dst = ktile + (key >> 3) * 8192 + (16 * SL + 4 * qd) * 128 + (key & 7) * 16;
-  if (src >= 0) {
+  if (src >= 0 && kFp8) {
+    store_fp8_dims(kb.v[2 * (SL & 1)], kb.v[2 * (SL & 1) + 1], wsc, dst);
+  } else if (src >= 0) {
     const uint32_t s = e4m3x2_f16x2(sc_pair);
     const uint32_t g0 = prmt(s, s, 0x1010u), g1 = prmt(s, s, 0x3232u);   // (scale, scale) of each group
 #pragma unroll
@@ -260,18 +302,7 @@ __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& k
     }
   } else if (src <= -2) {
     const uint8_t* wc = a.swa_codes + (-2 - (int64_t)src) * kD + 32 * qd + 128 * SL;
-    const uint4 cw[2] = {__ldg(reinterpret_cast<const uint4*>(wc)), __ldg(reinterpret_cast<const uint4*>(wc + 16))};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint4 c = cw[j >> 1];
-      const uint32_t w0 = word_of(c, (j & 1) * 2), w1 = word_of(c, (j & 1) * 2 + 1);
-      uint4 o;
-      o.x = win2_f16x2(w0 & 0xFFFFu, wsc);
-      o.y = win2_f16x2(w0 >> 16, wsc);
-      o.z = win2_f16x2(w1 & 0xFFFFu, wsc);
-      o.w = win2_f16x2(w1 >> 16, wsc);
-      *reinterpret_cast<uint4*>(dst + j * 128) = o;
-    }
+    store_fp8_dims(__ldg(reinterpret_cast<const uint4*>(wc)), __ldg(reinterpret_cast<const uint4*>(wc + 16)), wsc, dst);
   } else {
 #pragma unroll
     for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(dst + j * 128) = make_uint4(0, 0, 0, 0);
@@ -343,6 +374,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 
 
+template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
 k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -466,14 +498,14 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
     cur_src = key_source(a, row, b, kb0 + key, n_sel, sel_off, sel_cap, kb1, nv, w_first, pos0, qd == 0, status);
     if (qd == 0) {
       sm.slot[key] = cur_src;
-      sm.kexp[key] = (int8_t)(cur_src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)cur_src))) : 0);
+      sm.kexp[key] = (int8_t)key_exp<kFp8>(a, cur_src);
     }
     for (int c = qd + 1; c < n_my; c += 4) {
       const int32_t src =
           key_source(a, row, b, kb0 + c * kChunk + key, n_sel, sel_off, sel_cap, kb1, nv, w_first, pos0, true,
                      status);
       sm.slot[c * kChunk + key] = src;
-      sm.kexp[c * kChunk + key] = (int8_t)(src <= -2 ? window_exp(__ldg(a.swa_scales + (-2 - (int64_t)src))) : 0);
+      sm.kexp[c * kChunk + key] = (int8_t)key_exp<kFp8>(a, src);
     }
   }
   // ---- the first chunk's packed bytes
@@ -481,12 +513,14 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   uint2 cur_sc = make_uint2(0, 0);
   KeyBytes kb;
   if (!mma_warp && n_my > 0) {
-    load_slice<0>(a, cur_src, qd, kb);
-    load_slice<1>(a, cur_src, qd, kb);
-    load_slice<2>(a, cur_src, qd, kb);
-    load_slice<3>(a, cur_src, qd, kb);
-    cur_wsc = load_wscale(a, cur_src);
-    cur_sc = load_scales(a, cur_src, qd);
+    load_slice<0, kFp8>(a, cur_src, qd, kb);
+    load_slice<1, kFp8>(a, cur_src, qd, kb);
+    if (!kFp8) {
+      load_slice<2, kFp8>(a, cur_src, qd, kb);
+      load_slice<3, kFp8>(a, cur_src, qd, kb);
+      cur_sc = load_scales(a, cur_src, qd);
+    }
+    cur_wsc = load_wscale<kFp8>(a, cur_src);
   }
   tc::fence_async_smem();
   tc::tc_fence_before();
@@ -551,7 +585,9 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       const uint32_t w0 = __shfl_sync(0xffffffffu, cur_sc.x, (lane & 7) | (SL << 3));    \
       const uint32_t w1 = __shfl_sync(0xffffffffu, cur_sc.y, (lane & 7) | (SL << 3));    \
       const uint32_t pr = ((qd >> 1) ? w1 : w0) >> (16 * (qd & 1));                      \
-      if (wok) store_slice<SL>(a, kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile);   \
+      if (wok) store_slice<SL, kFp8>(a, kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile); \
+      /* FP8 rows: slices 2 and 3 of this chunk reuse the registers of 0 and 1 */        \
+      if (kFp8 && SL < 2) load_slice<(SL + 2) & 3, kFp8>(a, cur_src, qd, kb);            \
     }                                                                                    \
     tc::fence_async_smem();                                                              \
     __syncwarp();                                                                        \
@@ -564,16 +600,18 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 #undef CSA2_SLICE
       // the next chunk's bytes, requested together once this chunk's tile is written
       if (it + 1 < n_my) {
-        load_slice<0>(a, nxt_src, qd, kb);
-        load_slice<1>(a, nxt_src, qd, kb);
-        load_slice<2>(a, nxt_src, qd, kb);
-        load_slice<3>(a, nxt_src, qd, kb);
+        load_slice<0, kFp8>(a, nxt_src, qd, kb);
+        load_slice<1, kFp8>(a, nxt_src, qd, kb);
+        if (!kFp8) {
+          load_slice<2, kFp8>(a, nxt_src, qd, kb);
+          load_slice<3, kFp8>(a, nxt_src, qd, kb);
+        }
       }
       const bool valid = sm.slot[it * kChunk + kc] != -1;   // the softmax thread's key
       const int fk = sm.kexp[it * kChunk + kc];
       cur_src = nxt_src;
-      cur_wsc = load_wscale(a, nxt_src);
-      cur_sc = load_scales(a, nxt_src, qd);
+      cur_wsc = load_wscale<kFp8>(a, nxt_src);
+      if (!kFp8) cur_sc = load_scales(a, nxt_src, qd);
 
       // ---- softmax of the chunk: this thread's key, heads 16*hg .. +15
       wok = wok && warp_wait(&sm.bar_s, it & 1, abort);
@@ -797,7 +835,8 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s) {
   if (rows < sms && max_chunks > 1)
     n_split = (int)std::max<int64_t>(1, std::min<int64_t>(std::min(max_chunks, kMaxSplit), sms / rows));
   const size_t smem = sizeof(TcSmem);
-  e = cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kernel = a.kv_fp8 ? k_sparse_attn_tc<true> : k_sparse_attn_tc<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (rows * n_split >= ((int64_t)1 << 31)) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -814,7 +853,7 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, cudaStream_t s) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = n_split > 1 ? 2 : 1;
-  return counted(cudaLaunchKernelEx(&cfg, k_sparse_attn_tc, a, status_word(), n_split));
+  return counted(cudaLaunchKernelEx(&cfg, kernel, a, status_word(), n_split));
 }
 
 }  // namespace csa2

@@ -75,7 +75,9 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
                                   uint8_t* kv_codes, uint8_t* kv_scales,
                                   // optional indexer-key epilogue (compression)
                                   const float* idx_src, int64_t idx_row_stride, int Di,
-                                  int idx_dtype, void* idx_k, cudaStream_t s);
+                                  int idx_dtype, void* idx_k, cudaStream_t s,
+                                  // 1: FP8 main-KV rows (E4M3 codes [d], fp32 scale per entry)
+                                  int kv_fp8 = 0);
 // Window rows rebuilt from replayed tokens: row i of sequence b (latent = the
 // split sum of src row b * n_tok + i) gets RMSNorm, RoPE at raw position
 // tok_pos0[b] + i and the FP8 pack, into window row tok_pos0[b] + i - win_pos0[b].
@@ -185,6 +187,7 @@ struct AttnArgs {
   float scale;
   float* O;                   // [rows][Hq][d]
   float* lse;                 // [rows][Hq] or null
+  int kv_fp8;                 // main KV as FP8 rows (E4M3 [d] + fp32 scale per entry)
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t s);
 // ---- attention_tc.cu: tcgen05 kernel for d = 512 (every Hq and K + W the ABI admits)

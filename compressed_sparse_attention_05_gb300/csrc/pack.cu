@@ -187,8 +187,9 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
                  const int32_t* __restrict__ n_rows, const int32_t* __restrict__ page_table,
                  int max_pages, int64_t n_pages, uint8_t* __restrict__ kv_codes,
                  uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
-                 int Di, int idx_dtype, void* idx_k, const __grid_constant__ RopeTurns rope, uint32_t* status) {
-  __shared__ float row_buf[kNrpWarps][512];
+                 int Di, int idx_dtype, void* idx_k, int kv_fp8, const __grid_constant__ RopeTurns rope,
+                 uint32_t* status) {
+  __shared__ __align__(16) float row_buf[kNrpWarps][512];
   pdl_trigger();
   pdl_wait();
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -204,7 +205,10 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
   float v[16];
   load_latent(src, m, has, lane, v);
   norm_rope_row(v, has, d, r, gamma, eps, 4ull * (uint64_t)e + 3ull, rope, row_buf[warp], lane);
-  if (has) {
+  if (kv_fp8) {   // the FP8 main-KV format: R5's row rule, one fp32 scale per entry
+    __syncwarp();
+    fp8_row(row_buf[warp], d, kv_codes + slot * d, reinterpret_cast<float*>(kv_scales) + slot, lane);
+  } else if (has) {
     Mxfp4Group g = pack_group16(v);
     reinterpret_cast<uint2*>(kv_codes + slot * (d / 2))[lane] = g.codes;
     kv_scales[slot * (d / 16) + lane] = (uint8_t)g.scale;
@@ -308,14 +312,14 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
                                   const int32_t* page_table, int max_pages, int64_t n_pages,
                                   uint8_t* kv_codes, uint8_t* kv_scales, const float* idx_src,
                                   int64_t idx_row_stride, int Di, int idx_dtype, void* idx_k,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, int kv_fp8) {
   const int64_t rows = (int64_t)B * n_max;
   if (rows == 0) return cudaSuccess;
-  if (r < 0 || r / 2 > 256) return cudaErrorInvalidValue;
+  if (r < 0 || r / 2 > 256 || (kv_fp8 && d != 512)) return cudaErrorInvalidValue;
   const RopeTurns rope = rope_turns(r, rope_base);
   return launch_step(k_norm_rope_pack, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
       src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
-      n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, rope, status_word());
+      n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, kv_fp8, rope, status_word());
 }
 
 cudaError_t launch_norm_rope_fp8_window(LatentSource src, int B, int n_tok, int d, int r,

@@ -37,8 +37,13 @@ class LayerGroup:
         self.n_entries = torch.tensor([wl.entries_after(b) for b in range(B)], dtype=torch.int32, device=dev)
         self.max_entries = max(wl.entries_after(b) for b in range(B))
         n_slots = self.n_pages * 64
-        self.kv_codes = torch.zeros(n_slots, d // 2, dtype=torch.uint8, device=dev)
-        self.kv_scales = torch.zeros(n_slots, d // 16, dtype=torch.uint8, device=dev)
+        self.fp8kv = getattr(wl, "kv_format", "mxfp4") == "fp8"
+        if self.fp8kv:   # V4-style main KV: E4M3 row + fp32 scale per entry
+            self.kv_codes = torch.zeros(n_slots, d, dtype=torch.uint8, device=dev)
+            self.kv_scales = torch.zeros(n_slots, dtype=torch.float32, device=dev)
+        else:
+            self.kv_codes = torch.zeros(n_slots, d // 2, dtype=torch.uint8, device=dev)
+            self.kv_scales = torch.zeros(n_slots, d // 16, dtype=torch.uint8, device=dev)
         self.idx_k = torch.zeros(n_slots, Di, dtype=wl.idx_torch_dtype, device=dev)
         self.gamma = wl.gamma(dev)
         self._fill_cache()
@@ -113,7 +118,8 @@ class LayerGroup:
                 m = min(n, s + _CHUNK) - s
                 rows = torch.arange(s, s + m, dtype=torch.int64, device=dev)
                 lat = wl.cache_latent(b, rows).reshape(1, m, wl.d).contiguous()
-                abi.csa2_norm_rope_pack(
+                pack = abi.csa2_norm_rope_pack_fp8 if self.fp8kv else abi.csa2_norm_rope_pack
+                pack(
                     lat, wl.r, self.gamma, wl.eps, wl.rope_base,
                     torch.tensor([s], dtype=torch.int32, device=dev),
                     torch.tensor([m], dtype=torch.int32, device=dev),
@@ -127,7 +133,8 @@ class LayerGroup:
         return abi.Dims(B=wl.B, Tq=wl.Tq, d=wl.d, r=wl.r, Hq=wl.Hq, Hi=wl.Hi, Di=wl.Di,
                         idx_dtype=abi.CSA2_BF16 if wl.idx_dtype == "bf16" else abi.CSA2_F32, K=wl.K, W=wl.W,
                         max_pages=self.page_table.shape[1], n_pool_blocks=wl.pool_blocks,
-                        pool_block=wl.pool_block, swa_cap=wl.swa_cap)
+                        pool_block=wl.pool_block, swa_cap=wl.swa_cap,
+                        kv_format=abi.CSA2_KV_FP8 if self.fp8kv else abi.CSA2_KV_MXFP4)
 
     def cache(self) -> abi.Cache:
         return abi.Cache(kv_codes=self.kv_codes.data_ptr(), kv_scales=self.kv_scales.data_ptr(),

@@ -56,6 +56,7 @@ class Workload:
     rope_base: float = 10000.0
     eps: float = 1e-6
     replay_H: Optional[int] = None  # SWA Bounded Replay: hidden size of the replayed tokens
+    kv_format: str = "mxfp4"    # main KV: "mxfp4" (the pages' V4.1 format) or "fp8" (V4-style, for the A/B)
     description: str = ""
 
     # ---- derived structure -------------------------------------------------
@@ -253,6 +254,16 @@ def decode_128k(B: int = 32, L: int = 131072) -> Workload:
                                 f"{L // 4} entries each, Top-512, 64 heads, window 128")
 
 
+def decode_fp8kv_128k(B: int = 32, L: int = 131072) -> Workload:
+    """The decode workload with the V4-style FP8 main KV (E4M3 row + fp32 scale per
+    entry, 516 B against MXFP4's 288 B): the A/B of the storage format."""
+    wl = decode_128k(B, L)
+    wl.kv_format = "fp8"
+    wl.name = f"decode_fp8kv_{L // 1024}k_b{B}"
+    wl.description += ", FP8 main KV (516 B/entry)"
+    return wl
+
+
 def prefill_64k(n_new: int = 4096, ctx: int = 65536, H: int = 4096) -> Workload:
     """Chunked prefill, Full mode: n_new tokens ending a ctx-token context, compressed 4:1."""
     return Workload(name=f"prefill_full_{ctx // 1024}k_chunk{n_new}", seed=2, B=1,
@@ -339,6 +350,7 @@ def decoder_replay(B: int = 8, L: int = 131072, n_win: int = 128, H: int = 4096)
 ALL = {
     "tiny": tiny,
     "decode": decode_128k,
+    "decode_fp8kv": decode_fp8kv_128k,
     "prefill": prefill_64k,
     "hierarchical": hierarchical_1m,
     "ragged": ragged_serving,

@@ -38,6 +38,10 @@
  *     kv_codes  uint8 [n_pages][64][d/2]   E2M1 codes, channel 2i in the low
  *                                          nibble of byte i, 2i+1 in the high
  *     kv_scales uint8 [n_pages][64][d/16]  E4M3 scale codes, one per 16 channels
+ *   (dims.kv_format = CSA2_KV_FP8, the V4-style main KV kept for comparison:
+ *     kv_codes  uint8 [n_pages][64][d]     E4M3 codes
+ *     kv_scales fp32  [n_pages][64]        one scale per entry, R5's rule;
+ *     516 bytes per 512-d entry against MXFP4's 288.)
  *     idx_k     [n_pages][64][Di]          indexer keys (bf16 or fp32)
  *   page_table int32 [B][max_pages]: physical page of logical page p of
  *     sequence b; entry j of sequence b lives in page page_table[b][j/64],
@@ -118,6 +122,10 @@ extern "C" {
 #define CSA2_F32 0
 #define CSA2_BF16 1
 
+/* main-KV formats (dims.kv_format) */
+#define CSA2_KV_MXFP4 0 /* E2M1 codes + E4M3 scale per 16 channels (V4.1, the pages' format) */
+#define CSA2_KV_FP8 1   /* E4M3 codes + fp32 scale per entry (V4-style, for the A/B)       */
+
 /* layer modes (static per layer) */
 #define CSA2_MODE_FULL 0    /* compute KV (optional), score all, Top-K   */
 #define CSA2_MODE_REINDEX 1 /* rescore the Full layer's pool, Top-K      */
@@ -130,7 +138,7 @@ extern "C" {
 #define CSA2_STATUS_TIMEOUT 8u      /* a bounded on-chip wait gave up; outputs of that launch are invalid */
 
 /* ABI version of this header (bumped on any incompatible change). */
-#define CSA2_ABI_VERSION 1
+#define CSA2_ABI_VERSION 2
 
 int csa2_abi_version(void);
 
@@ -162,12 +170,13 @@ typedef struct csa2_dims {
   int32_t n_pool_blocks; /* hierarchical pool: blocks kept (2048)          */
   int32_t pool_block;    /* hierarchical pool: entries per block (8)       */
   int32_t swa_cap;       /* rows per sequence in the window buffers        */
+  int32_t kv_format;     /* CSA2_KV_MXFP4 (0) or CSA2_KV_FP8 (FP8 needs d = 512) */
 } csa2_dims;
 
 /* The shared compressed cache of one layer group. */
 typedef struct csa2_cache {
-  uint8_t* kv_codes;         /* [n_pages][64][d/2]                           */
-  uint8_t* kv_scales;        /* [n_pages][64][d/16]                          */
+  uint8_t* kv_codes;         /* [n_pages][64][d/2] (FP8: [n_pages][64][d])   */
+  uint8_t* kv_scales;        /* [n_pages][64][d/16] (FP8: fp32 [n_pages][64]) */
   void* idx_k;               /* [n_pages][64][Di], idx_dtype                 */
   const int32_t* page_table; /* [B][max_pages]                               */
   const int32_t* n_entries;  /* [B] entries present (device)                 */
@@ -207,6 +216,18 @@ int csa2_norm_rope_pack(const float* latent, int32_t B, int32_t n_max, int32_t d
                         const int32_t* first_entry, const int32_t* n_rows,
                         const int32_t* page_table, int32_t max_pages, int64_t n_pages,
                         uint8_t* kv_codes, uint8_t* kv_scales, void* stream);
+
+/* The same for the FP8 main-KV format (dims.kv_format = CSA2_KV_FP8): after
+ * RMSNorm and RoPE each entry row is packed by R5's rule (scale = amax / 448,
+ * stored fp32; codes = E4M3_rne_satfinite(x / scale)) into kv_codes uint8
+ * [n_pages][64][d] and kv_scales fp32 [n_pages][64].  The V4 review and the
+ * V4.1 analysis (§03) describe V4's main KV as FP8; this format exists to
+ * compare the two on the same path.  d = 512 only. */
+int csa2_norm_rope_pack_fp8(const float* latent, int32_t B, int32_t n_max, int32_t d, int32_t r,
+                            const float* gamma, float eps, float rope_base,
+                            const int32_t* first_entry, const int32_t* n_rows,
+                            const int32_t* page_table, int32_t max_pages, int64_t n_pages,
+                            uint8_t* kv_codes, float* kv_scales, void* stream);
 
 /* ---- a1-a4: compress new tokens into the paged cache ----------------------
  * hidden bf16 [B][T][H] (the new tokens of every sequence, token 0 at raw

@@ -90,8 +90,23 @@ def norm_rope_pack(latent: np.ndarray, entry_ids: np.ndarray, gamma, eps, r, bas
     return x, codes, scales
 
 
+def norm_rope_pack_fp8(latent: np.ndarray, entry_ids: np.ndarray, gamma, eps, r, base):
+    """Steps a2 and the V4-style FP8 main-KV pack on given latent rows: returns
+    (post-RoPE fp32 x, E4M3 codes [n, d], fp32 scales [n]).
+
+    The same RMSNorm and RoPE as the MXFP4 entries; the row is then packed by the
+    FP8 rule of the sliding window (one scale per row, amax / 448).  The DeepSeek V4
+    review and the V4.1 analysis (§03, V4.1's FP4 main KV halves V4's FP8 one)
+    describe this format only as V4's; it is kept to compare the two.
+    """
+    x = rmsnorm(latent, gamma, eps)
+    x = rope(x, entry_position(entry_ids), r, base)
+    codes, scales = formats.fp8_pack(x.astype(np.float32))
+    return x, codes, scales
+
+
 def compress_pack(hidden, W, gamma, eps, r, base, first_entry: int, W_idx=None,
-                  idx_dtype: str = "bf16"):
+                  idx_dtype: str = "bf16", kv_format: str = "mxfp4"):
     """Steps a1-a4 for one sequence's new tokens [T, H] (T a multiple of 4 or not).
 
     Returns a dict with the fp32 latent c, the post-RoPE x, the MXFP4 codes and
@@ -100,7 +115,8 @@ def compress_pack(hidden, W, gamma, eps, r, base, first_entry: int, W_idx=None,
     """
     c = compress(hidden, W)
     ids = first_entry + np.arange(c.shape[0])
-    x, codes, scales = norm_rope_pack(c, ids, gamma, eps, r, base)
+    pack = norm_rope_pack_fp8 if kv_format == "fp8" else norm_rope_pack
+    x, codes, scales = pack(c, ids, gamma, eps, r, base)
     out = {"c": c, "x": x, "codes": codes, "scales": scales, "entry_ids": ids}
     if W_idx is not None:
         k = concat_groups(hidden) @ np.asarray(W_idx, dtype=np.float64).T

@@ -43,6 +43,7 @@ class SequenceState:
         self.n_before = wl.entries_before(b)
         self.n_after = wl.entries_after(b)
         self.gamma = _np(wl.gamma())
+        self.kv_format = getattr(wl, "kv_format", "mxfp4")
         self._new = None
         self._idx_k = None
         self._replay = {}
@@ -54,7 +55,8 @@ class SequenceState:
             hid = _np(wl.hidden()[self.b])
             self._new = compress.compress_pack(
                 hid, _np(wl.w_compress()), self.gamma, wl.eps, wl.r, wl.rope_base,
-                first_entry=self.n_before, W_idx=_np(wl.w_index()), idx_dtype=wl.idx_dtype)
+                first_entry=self.n_before, W_idx=_np(wl.w_index()), idx_dtype=wl.idx_dtype,
+                kv_format=self.kv_format)
         return self._new
 
     def indexer_keys(self) -> np.ndarray:
@@ -68,16 +70,20 @@ class SequenceState:
         return self._idx_k
 
     def packed_rows(self, rows: np.ndarray):
-        """(codes, scales) of entries ``rows``: cached ones packed from the raw latent."""
+        """(codes, scales) of entries ``rows``: cached ones packed from the raw latent.
+
+        MXFP4: codes [n, d/2], scales [n, d/16] (E4M3 codes); FP8 main KV: codes
+        [n, d] (E4M3), scales [n] (fp32)."""
         rows = np.asarray(rows, dtype=np.int64)
         wl = self.wl
-        codes = np.zeros((len(rows), wl.d // 2), np.uint8)
-        scales = np.zeros((len(rows), wl.d // 16), np.uint8)
+        fp8 = self.kv_format == "fp8"
+        codes = np.zeros((len(rows), wl.d if fp8 else wl.d // 2), np.uint8)
+        scales = np.zeros(len(rows), np.float32) if fp8 else np.zeros((len(rows), wl.d // 16), np.uint8)
         old = rows < self.n_before
         if old.any():
             lat = _np(wl.cache_latent(self.b, torch.from_numpy(rows[old])))
-            _, c, s = compress.norm_rope_pack(lat, rows[old], self.gamma, wl.eps, wl.r,
-                                              wl.rope_base)
+            pack = compress.norm_rope_pack_fp8 if fp8 else compress.norm_rope_pack
+            _, c, s = pack(lat, rows[old], self.gamma, wl.eps, wl.r, wl.rope_base)
             codes[old], scales[old] = c, s
         if (~old).any():
             new = self.new_entries()
@@ -87,6 +93,8 @@ class SequenceState:
 
     def kv_rows(self, rows) -> np.ndarray:
         c, s = self.packed_rows(rows)
+        if self.kv_format == "fp8":
+            return formats.fp8_unpack_bf16(c, s)
         return formats.mxfp4_unpack(c, s)
 
     def replay_rows(self, layer: int):

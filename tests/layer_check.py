@@ -70,16 +70,18 @@ class Operands:
         cg = self.g.kv_codes[sl].cpu().numpy()
         sg = self.g.kv_scales[sl].cpu().numpy()
         co, so = self.st.packed_rows(rows)
-        diff = np.any(cg != co, axis=1) | np.any(sg != so, axis=1)
+        fp8 = self.g.fp8kv
+        diff = np.any(cg != co, axis=1) | (sg != so if fp8 else np.any(sg != so, axis=1))
         old = diff & (rows < self.st.n_before)
-        if old.any():   # packed by csa2_norm_rope_pack from a given latent: fp32 rounding only
+        if old.any():   # packed by csa2_norm_rope_pack(_fp8) from a given latent: fp32 rounding only
             wl = self.wl
             lat = _np(wl.cache_latent(self.b, torch.from_numpy(rows[old])))
             x, _, _ = Cm.norm_rope_pack(lat, rows[old], self.st.gamma, wl.eps, wl.r, wl.rope_base)
             tau = parity.latent_error_bound(lat, np.zeros_like(lat), self.st.gamma, wl.eps, wl.r, x)
-            parity.check_mxfp4_after_gemm(cg[old], sg[old], x, tau)
+            check = parity.check_fp8_after_gemm if fp8 else parity.check_mxfp4_after_gemm
+            check(cg[old], sg[old], x, tau)
         assert not (diff & (rows >= self.st.n_before)).any() or self.new is not None
-        return F.mxfp4_unpack(cg, sg)
+        return F.fp8_unpack_bf16(cg, sg) if fp8 else F.mxfp4_unpack(cg, sg)
 
 
 def check_group(wl, samples, group=None):
@@ -143,7 +145,7 @@ _BOUNDS = {}
 def compressed_entry_bounds(wl, b):
     """(oracle post-RoPE rows x, their error bound tau_x, exact indexer keys, their bound)
     of the entries this step compresses for sequence b."""
-    key = (wl.name, wl.seed, wl.B, wl.n_new, wl.H, tuple(wl.t_first), b)
+    key = (wl.name, wl.seed, wl.B, wl.n_new, wl.H, tuple(wl.t_first), wl.kv_format, b)
     if key not in _BOUNDS:
         st = OL.SequenceState(wl, b)
         new = st.new_entries()
@@ -156,13 +158,17 @@ def compressed_entry_bounds(wl, b):
 
 
 def check_compressed_entries(g, wl, b):
-    """Entries packed by this step's compression (GEMM + RMSNorm/RoPE/MXFP4 epilogue)
-    and their indexer keys, byte for byte against the oracle under the boundary rule
-    of parity.check_mxfp4_after_gemm / check_keys_after_gemm.  Returns the flips."""
+    """Entries packed by this step's compression (GEMM + RMSNorm/RoPE/MXFP4 or FP8
+    epilogue) and their indexer keys, byte for byte against the oracle under the
+    boundary rules of parity.check_mxfp4_after_gemm (check_fp8_after_gemm for the
+    FP8 main KV) / check_keys_after_gemm.  Returns the flips."""
     new, tau_x, k_exact, tau_k = compressed_entry_bounds(wl, b)
     ids = torch.from_numpy(new["entry_ids"])
     slots = (g.page_table[b, ids // 64].long().cpu() * 64 + ids % 64).cuda()
-    fs, fc = parity.check_mxfp4_after_gemm(g.kv_codes[slots].cpu().numpy(), g.kv_scales[slots].cpu().numpy(),
-                                           new["x"], tau_x)
+    cg, sg = g.kv_codes[slots].cpu().numpy(), g.kv_scales[slots].cpu().numpy()
+    if g.fp8kv:
+        fs, fc = 0, parity.check_fp8_after_gemm(cg, sg, new["x"], tau_x)
+    else:
+        fs, fc = parity.check_mxfp4_after_gemm(cg, sg, new["x"], tau_x)
     fk = parity.check_keys_after_gemm(g.idx_k[slots].float().cpu().double().numpy(), k_exact, tau_k, wl.idx_dtype)
     return fs, fc, fk

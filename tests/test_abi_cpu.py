@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert abi.csa2_abi_version() == 1
+    assert abi.csa2_abi_version() == 2
 
 
 FAKE = 1 << 20  # an aligned non-null address; validation fails before any use

@@ -25,6 +25,11 @@ def _decode():
     return WL.decode_128k(B=4, L=4 * 30000 + 1)
 
 
+def _decode_fp8kv():
+    wl = WL.decode_fp8kv_128k(B=4, L=4 * 30000 + 1)
+    return wl
+
+
 def _prefill():
     return WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
 
@@ -42,7 +47,8 @@ def _snapshot(g):
     return out
 
 
-@pytest.mark.parametrize("make", [_decode, _prefill, _hierarchical], ids=["decode", "prefill", "hierarchical"])
+@pytest.mark.parametrize("make", [_decode, _decode_fp8kv, _prefill, _hierarchical],
+                         ids=["decode", "decode_fp8kv", "prefill", "hierarchical"])
 def test_step_bits_repeat(make):
     wl = make()
     g = harness.LayerGroup(wl)

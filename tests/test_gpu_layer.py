@@ -49,6 +49,25 @@ def test_decode_small_k1024():
     check_group(wl, [(0, 0), (1, 0), (2, 0)])
 
 
+def test_decode_small_fp8kv():
+    """The V4-style FP8 main KV: the packer writes E4M3 rows with fp32 scales and the
+    attention kernel dequantises them as it does the window rows."""
+    wl = _decode_small()
+    wl.kv_format = "fp8"
+    wl.name = "decode_small_fp8kv"
+    g, _ = check_group(wl, [(0, 0), (1, 0), (2, 0)])
+    assert g.kv_codes.shape[1] == wl.d and g.kv_scales.dtype == torch.float32
+
+
+def test_prefill_small_with_compression_fp8kv():
+    """Compression GEMM with the FP8 epilogue, then attention over FP8 entries."""
+    wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
+    wl.kv_format = "fp8"
+    wl.name = "prefill_small_fp8kv"
+    g, _ = check_group(wl, [(0, i) for i in (0, 1, 2, 3, 100, 255)])
+    check_compressed_entries(g, wl, 0)
+
+
 def test_prefill_small_with_compression():
     wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
     g, _ = check_group(wl, [(0, i) for i in (0, 1, 2, 3, 4, 100, 254, 255)])
@@ -163,6 +182,11 @@ def test_index_scores_many_queries():
 def test_full_decode_128k_b32():
     wl = WL.decode_128k()
     check_group(wl, [(0, 0), (31, 0)])
+
+
+def test_full_decode_fp8kv_128k_b32():
+    wl = WL.decode_fp8kv_128k()
+    check_group(wl, [(0, 0), (17, 0), (31, 0)])
 
 
 def test_full_hierarchical_1m_b8():

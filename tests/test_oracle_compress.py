@@ -133,3 +133,33 @@ def test_synthetic_latent_max_near_observed_value():
     # the pages observe a largest magnitude around 10 after normalisation
     obs = PAGE["latent_observed_max"]["value"]
     assert 0.5 * obs < np.abs(x).max() < 2 * obs
+
+
+def test_fp8_main_kv_pack_pipeline_and_error_bound():
+    """V4-style FP8 main KV (kept for the A/B against MXFP4): the same RMSNorm + RoPE
+    row, packed as E4M3 codes with one fp32 scale per entry (amax / 448)."""
+    T, H, d, r = 64, 16, 512, 64
+    g = np.random.default_rng(11)
+    h = g.normal(0, 1, (T, H))
+    W = g.normal(0, 0.3, (d, 4 * H))
+    gamma = 1.0 + 0.1 * g.standard_normal(d)
+    out = C.compress_pack(h, W, gamma, 1e-6, r, 1e4, first_entry=37, kv_format="fp8")
+    mx = C.compress_pack(h, W, gamma, 1e-6, r, 1e4, first_entry=37)
+    assert np.array_equal(out["x"], mx["x"])          # the format changes only the pack
+    x = out["x"]
+    assert out["codes"].shape == (T // 4, d) and out["scales"].dtype == np.float32
+    # 516 bytes per entry (512 codes + one fp32 scale) against MXFP4's 288
+    assert out["codes"][0].nbytes + out["scales"][:1].nbytes == 516
+    assert mx["codes"][0].nbytes + mx["scales"][0].nbytes == PAGE["mxfp4_bytes_per_entry_d512"]["value"]
+    # each row's largest magnitude lands on E4M3's largest finite value
+    assert np.all(np.max(F.E4M3_TABLE[out["codes"] & 0x7F], axis=1) == PAGE["e4m3_max"]["value"])
+    # error of one E4M3 rounding (3 mantissa bits: half a step is 2^-4 relative; below
+    # the normal range half the 2^-9 subnormal step, scaled) then one bf16 rounding
+    deq = F.fp8_unpack_bf16(out["codes"], out["scales"])
+    s = out["scales"].astype(np.float64)[:, None]
+    bound = (2.0 ** -4 * np.abs(x) + 2.0 ** -10 * s) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(x)
+    assert np.all(np.abs(deq - x) <= bound)
+    # FP8 is the finer format: its error is well under MXFP4's on the same rows
+    e8 = np.abs(deq - x).mean()
+    e4 = np.abs(F.mxfp4_unpack(mx["codes"], mx["scales"]) - x).mean()
+    assert e8 < 0.5 * e4
