@@ -360,8 +360,8 @@ __device__ __forceinline__ void load_scores(uint32_t tm, int hg, uint32_t lane_q
 // Bounded wait of a whole warp; on time-out the CTA's abort flag is raised.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   bool ok = false;
-  for (uint32_t i = 0; i < (1u << 22); ++i) {
-    if (tc::mbar_try_wait(bar, parity)) {
+  for (uint32_t i = 0; i < (1u << 21); ++i) {   // <= 2^21 suspensions of <= 1 us
+    if (tc::mbar_try_wait_sleep(bar, parity, 1000)) {
       ok = true;
       break;
     }

@@ -191,7 +191,7 @@ k_index_scores_mma(IndexerArgs a, int QG, float* __restrict__ scores, int64_t st
 // pages per SM stay in flight, which is what an HBM-bound scan needs.
 // Every wait is bounded; on a timeout the CTA raises CSA2_STATUS_TIMEOUT,
 // drains the copies it issued and exits.
-constexpr int kScanStages = 6;
+constexpr int kScanStages = 3;   // 4 CTAs per SM: the scoring warps, not the copies, set the pace
 constexpr int kScanConsumers = 4;
 constexpr int kScanThreads = (kScanConsumers + 1) * 32;
 constexpr int kPageBytes = kPage * 128 * 2;
@@ -205,8 +205,8 @@ struct ScanShared {
 
 // Waits for `parity` on `bar` while no other role has aborted.
 __device__ __forceinline__ bool scan_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < (1u << 22); ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < (1u << 21); ++i) {   // <= 2^21 suspensions of <= 1 us
+    if (tc::mbar_try_wait_sleep(bar, parity, 1000)) return true;
     if ((i & 255) == 255 && *abort) return false;
   }
   *abort = 1;
@@ -319,6 +319,7 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
     };
     int cur = page_id(p0 + lane), nxt = page_id(p0 + 32 + lane);
     int issued = 0;
+    const uint64_t stream_policy = tc::l2_evict_first_policy();   // keys are read once
     for (int i = 0; i < n_pages; ++i) {
       if (i > 0 && (i & 31) == 0) {
         cur = nxt;
@@ -337,9 +338,9 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
         } else {
           ss.valid[st] = 1;
           tc::mbar_arrive_expect_tx(&ss.full[st], kPageBytes);
-          tc::bulk_g2s(ring + st * kPageBytes,
-                       reinterpret_cast<const unsigned char*>(a.k) + (int64_t)pg * kPageBytes, kPageBytes,
-                       &ss.full[st]);
+          tc::bulk_g2s_hint(ring + st * kPageBytes,
+                            reinterpret_cast<const unsigned char*>(a.k) + (int64_t)pg * kPageBytes, kPageBytes,
+                            &ss.full[st], stream_policy);
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;

@@ -620,24 +620,31 @@ k_topk_hist(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k
 
 // ---- few rows with a given histogram, each spread over a cluster -------------------------
 // Decode: 32 rows of 32,768 scores would keep 32 SMs busy.  A cluster of
-// kTopkRanks CTAs takes one row: every rank locates the threshold bin from
-// the row's histogram itself, classifies its quarter of the row (float
-// compares with the bin's edges) and writes the selection bits and the
-// threshold bin's candidates into rank 0's shared memory (distributed
-// shared-memory reductions and stores); rank 0 then finishes as k_topk does.
+// kTopkRanks CTAs takes one row, rank r a contiguous quarter of it.  Every
+// rank locates the threshold bin from the row's histogram while its quarter
+// loads, counts its entries above the bin and sends the bin's candidates
+// (key, index) and that count to every rank of the cluster (distributed
+// shared-memory stores, then one cluster barrier).  From then on each rank
+// works alone on identical data: the exact K-th key among all candidates (two
+// radix passes of 11 and 10 bits), the ties taken (the lowest indices), every
+// rank's selected count and so its own output offset; it then writes its
+// quarter's selection in index order.  The ranks' outputs are contiguous runs
+// of one ascending list.
 constexpr int kTopkRanks = 4;
-constexpr int kClusterMaxN = kTopkRanks * kTopkThreads * 8;   // 8 entries per thread and rank
-constexpr int kClusterCap = 4096;
+constexpr int kClThreads = 1024;                             // threads per rank
+constexpr int kClPer = 8;                                    // contiguous entries per thread
+constexpr int kClusterMaxN = kTopkRanks * kClThreads * kClPer;
+constexpr int kClusterCap = 2048;   // candidates of the threshold bin, all ranks together
 
 struct TopkClusterSmem {
   uint32_t hist[2048];
-  uint32_t hist2[256];
+  uint32_t hist2[2048];
   int warp_tot[kTopkWarps];
-  int nC, pad_;
-  uint32_t ckey[kClusterCap];
-  int32_t cidx[kClusterCap];
-  uint32_t sel_bits[kClusterMaxN / 32];
-  uint32_t tie_bits[kClusterMaxN / 32];
+  int n_above[kTopkRanks];   // entries above the bin in rank r's quarter (sent by rank r)
+  int n_cand[kTopkRanks];    // candidates of rank r's quarter (sent by rank r)
+  int local_above, local_cand, tie_idx, bstar, need, n_tie, off;
+  uint32_t T;
+  uint2 cand[kTopkRanks][kClusterCap];   // (key, index); segment r filled by rank r
 };
 
 __device__ __forceinline__ uint32_t cl_rank() {
@@ -650,26 +657,75 @@ __device__ __forceinline__ uint32_t cl_map(const void* p, uint32_t rank) {   // 
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
   return r;
 }
+// Split cluster barrier: arrive early (no ordering), wait before the first
+// remote store (every CTA of the cluster has then started).
+__device__ __forceinline__ void cl_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cl_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cl_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cl_red_or(uint32_t addr, uint32_t v) {
-  asm volatile("red.shared::cluster.or.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t cl_atom_add(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-  return old;
 }
 __device__ __forceinline__ void cl_st(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void cl_st2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+// One warp: the digit of a BINS-bin histogram (BINS = 64 m) that holds the
+// need-th largest element, and the count in the digits above it.  Two levels of
+// warp scans: lane l first sums the BINS/32 digits of chunk l (chunk 0 = the
+// highest digits), then the chunk that holds the element is split over the lanes
+// two digits each.  No block barrier.
+template <int BINS>
+__device__ __forceinline__ int warp_find_digit(const uint32_t* hist, int need, int* above_out) {
+  constexpr int PER = BINS / 32;
+  const int lane = threadIdx.x & 31;
+  const int hi = BINS - PER * lane;   // lane's chunk: digits [hi - PER, hi)
+  const uint4* h4 = reinterpret_cast<const uint4*>(hist + hi - PER);
+  int c = 0;
+#pragma unroll
+  for (int q = 0; q < PER / 4; ++q) {
+    const uint4 w = h4[q];
+    c += (int)(w.x + w.y + w.z + w.w);
+  }
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  uint32_t hit = __ballot_sync(0xffffffffu, incl - c < need && incl >= need);
+  const int L = hit ? __ffs(hit) - 1 : 31;
+  int cum = __shfl_sync(0xffffffffu, incl - c, L);   // elements above chunk L
+  // chunk L, highest digits first: lane l takes digits top - 2l and top - 2l - 1
+  const int top = BINS - PER * L - 1 - 2 * lane;
+  const int ha = 2 * lane < PER ? (int)hist[top] : 0;
+  const int hb = 2 * lane + 1 < PER ? (int)hist[top - 1] : 0;
+  int c2 = ha + hb, incl2 = c2;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl2, o);
+    if (lane >= o) incl2 += t;
+  }
+  const int before = cum + incl2 - c2;
+  hit = __ballot_sync(0xffffffffu, before < need && before + c2 >= need);
+  const int L2 = hit ? __ffs(hit) - 1 : 0;
+  const int first = before + ha >= need;   // the element lies in the higher of the two digits
+  const int dg = __shfl_sync(0xffffffffu, first ? top : top - 1, L2);
+  *above_out = __shfl_sync(0xffffffffu, first ? before : before + ha, L2);
+  return dg;
+}
 
 template <bool kVec>
-__global__ void __launch_bounds__(kTopkThreads, 1)
+__global__ void __launch_bounds__(kClThreads, 1)
 k_topk_cluster(const float* __restrict__ scores, int64_t stride, ValidSpec v, int k, int32_t* __restrict__ out_idx,
                int32_t* __restrict__ out_cnt, Remap remap, const uint32_t* __restrict__ hist_in,
                int64_t hist_stride) {
+  constexpr int NT = kClThreads;
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -683,22 +739,24 @@ k_topk_cluster(const float* __restrict__ scores, int64_t stride, ValidSpec v, in
   const int tid = threadIdx.x, lane = tid & 31;
   // every rank takes the same early exits: they depend on the row only
   if (rank == 0) {
-    for (int j = kk + tid; j < k; j += kTopkThreads) out[j] = -1;
+    for (int j = kk + tid; j < k; j += NT) out[j] = -1;
     if (tid == 0) out_cnt[row] = kk;
   }
   if (kk == 0) return;
   if (kk == n) {
     if (rank == 0)
-      for (int j = tid; j < n; j += kTopkThreads) out[j] = remap_index(remap, row, j);
+      for (int j = tid; j < n; j += NT) out[j] = remap_index(remap, row, j);
     return;
   }
-  // this rank's quarter of the row (a multiple of 4 entries: float4 aligned)
+  // this rank's quarter of the row (a multiple of 4 entries: float4 aligned); thread
+  // tid holds the kClPer entries j0 .. j0 + kClPer - 1 (index order = thread order)
   const int part = ((n + 4 * kTopkRanks - 1) / (4 * kTopkRanks)) * 4;
   const int q0 = min(n, (int)rank * part), q1 = min(n, q0 + part);
-  float x[8];
+  const int j0 = q0 + kClPer * tid;
+  float x[kClPer];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {   // entries q0 + 4 (u * kTopkThreads + tid) .. +3
-    const int j = q0 + 4 * (u * kTopkThreads + tid);
+  for (int u = 0; u < kClPer; u += 4) {
+    const int j = j0 + u;
     float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
     if (kVec && j + 3 < q1) {
       f = *reinterpret_cast<const float4*>(s + j);
@@ -708,39 +766,46 @@ k_topk_cluster(const float* __restrict__ scores, int64_t stride, ValidSpec v, in
       if (j + 2 < q1) f.z = s[j + 2];
       if (j + 3 < q1) f.w = s[j + 3];
     }
-    x[4 * u] = f.x; x[4 * u + 1] = f.y; x[4 * u + 2] = f.z; x[4 * u + 3] = f.w;
+    x[u] = f.x; x[u + 1] = f.y; x[u + 2] = f.z; x[u + 3] = f.w;
   }
-  if (rank == 0) {
-    const int words = (n + 31) / 32;
-    for (int i = tid; i < words; i += kTopkThreads) {
-      sm.sel_bits[i] = 0;
-      sm.tie_bits[i] = 0;
-    }
-    if (tid == 0) sm.nC = 0;
+  for (int i = tid; i < 2048; i += NT) sm.hist[i] = hist_in[row * hist_stride + i];
+  if (tid == 0) {
+    sm.local_above = 0;
+    sm.local_cand = 0;
+    sm.tie_idx = 0x7FFFFFFF;
   }
-  for (int i = tid; i < 2048; i += kTopkThreads) sm.hist[i] = hist_in[row * hist_stride + i];
   __syncthreads();
-  int above;
-  const int bstar = find_digit_t<kTopkThreads>(sm.hist, 2048, kk, sm.warp_tot, &above);
-  const int need = kk - above;
+  if (tid < 32) {
+    int ab;
+    const int d = warp_find_digit<2048>(sm.hist, kk, &ab);
+    if (tid == 0) {
+      sm.bstar = d;
+      sm.need = kk - ab;
+    }
+  }
+  __syncthreads();
+  const int bstar = sm.bstar;
+  int need = sm.need;
   if ((int)sm.hist[bstar] > kClusterCap) {   // crowded bin (same decision on every rank)
-    if (rank == 0) radix_whole_row<kTopkThreads>(sm, s, n, kk, bstar, need, out, remap, row);
+    if (rank == 0) radix_whole_row<NT>(sm, s, n, kk, bstar, need, out, remap, row);
     return;
   }
-  const float f_lo = bstar == 0 ? -INFINITY : key_float((uint32_t)bstar << 21);
-  const float f_hi = bstar == 2047 ? __uint_as_float(0x7FFFFFFFu) : key_float((uint32_t)(bstar + 1) << 21);
-  cl_sync();   // rank 0's bitmaps and counter are cleared
-  const uint32_t r_sel = cl_map(sm.sel_bits, 0), r_nc = cl_map(&sm.nC, 0);
-  const uint32_t r_key = cl_map(sm.ckey, 0), r_idx = cl_map(sm.cidx, 0);
+  cl_arrive_relaxed();
+
+  // ---- classify the quarter: above the bin, or a candidate of the bin
+  int my_above = 0;
   uint32_t cm = 0;
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int j = q0 + 4 * ((u >> 2) * kTopkThreads + tid) + (u & 3);
-    if (j < q1) {
-      if (x[u] >= f_hi) cl_red_or(r_sel + 4u * (uint32_t)(j >> 5), 1u << (j & 31));
-      else if (x[u] >= f_lo) cm |= 1u << u;
+  for (int u = 0; u < kClPer; ++u) {
+    if (j0 + u < q1) {
+      const int bin = (int)(order_key(x[u]) >> 21);
+      my_above += bin > bstar;
+      if (bin == bstar) cm |= 1u << u;
     }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
+  if (lane == 0 && my_above) atomicAdd(&sm.local_above, my_above);
   const int c = __popc(cm);
   int incl = c;
 #pragma unroll
@@ -749,26 +814,122 @@ k_topk_cluster(const float* __restrict__ scores, int64_t stride, ValidSpec v, in
     if (lane >= o) incl += t;
   }
   const int wtot = __shfl_sync(0xffffffffu, incl, 31);
-  if (wtot) {
-    int base = 0;
-    if (lane == 31) base = (int)cl_atom_add(r_nc, (uint32_t)wtot);
-    base = __shfl_sync(0xffffffffu, base, 31);
-    int pos = base + incl - c;
+  int base = 0;
+  if (lane == 31 && wtot) base = atomicAdd(&sm.local_cand, wtot);
+  int pos = __shfl_sync(0xffffffffu, base, 31) + incl - c;
+  cl_wait();   // every CTA of the cluster has started: its shared memory may be written
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      if ((cm >> u) & 1u) {
-        if (pos < kClusterCap) {
-          cl_st(r_key + 4u * (uint32_t)pos, order_key(x[u]));
-          cl_st(r_idx + 4u * (uint32_t)pos, (uint32_t)(q0 + 4 * ((u >> 2) * kTopkThreads + tid) + (u & 3)));
-        }
-        ++pos;
+  for (int u = 0; u < kClPer; ++u) {
+    if ((cm >> u) & 1u) {
+      if (pos < kClusterCap) {
+#pragma unroll
+        for (int r = 0; r < kTopkRanks; ++r)
+          cl_st2(cl_map(&sm.cand[rank][pos], (uint32_t)r), order_key(x[u]), (uint32_t)(j0 + u));
       }
+      ++pos;
     }
   }
-  cl_sync();   // every rank's bits and candidates are in rank 0
-  if (rank != 0) return;
-  finish_from_candidates<kTopkThreads, TopkClusterSmem, true>(sm, n, kk, bstar, need, min(sm.nC, kClusterCap), out,
-                                                               remap, row);
+  __syncthreads();
+  if (tid < kTopkRanks) {
+    cl_st(cl_map(&sm.n_above[rank], (uint32_t)tid), (uint32_t)sm.local_above);
+    cl_st(cl_map(&sm.n_cand[rank], (uint32_t)tid), (uint32_t)min(sm.local_cand, kClusterCap));
+  }
+  cl_sync();   // every rank's counts and candidates are in every rank
+
+  // ---- the exact K-th key T among the candidates: bits 20..10, then 9..0 (block-wide
+  // histograms, one warp locates the digit), the ties taken and this rank's offset
+  for (int i = tid; i < 2048; i += NT) sm.hist2[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kTopkRanks; ++r)
+    for (int i = tid; i < sm.n_cand[r]; i += NT) red_add_shared(&sm.hist2[(sm.cand[r][i].x >> 10) & 2047u], 1u);
+  __syncthreads();
+  if (tid < 32) {
+    int ab;
+    const int d1 = warp_find_digit<2048>(sm.hist2, need, &ab);
+    if (tid == 0) {
+      sm.T = ((uint32_t)bstar << 11) | (uint32_t)d1;   // key >> 10 of the K-th key
+      sm.need = need - ab;
+    }
+  }
+  __syncthreads();
+  const uint32_t hi21 = sm.T;
+  need = sm.need;
+  for (int i = tid; i < 1024; i += NT) sm.hist2[i] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < kTopkRanks; ++r)
+    for (int i = tid; i < sm.n_cand[r]; i += NT) {
+      const uint32_t key = sm.cand[r][i].x;
+      if ((key >> 10) == hi21) red_add_shared(&sm.hist2[key & 1023u], 1u);
+    }
+  __syncthreads();
+  if (tid < 32) {
+    int ab;
+    const int d2 = warp_find_digit<1024>(sm.hist2, need, &ab);
+    if (tid == 0) {
+      sm.T = (hi21 << 10) | (uint32_t)d2;
+      sm.need = need - ab;                  // entries equal to T that are taken (>= 1)
+      sm.n_tie = (int)sm.hist2[d2];
+      int off = 0;
+      for (int r = 0; r < (int)rank; ++r) off += sm.n_above[r];
+      sm.off = off;
+    }
+  }
+  __syncthreads();
+  const uint32_t T = sm.T;
+  need = sm.need;
+  if (need < sm.n_tie) {
+    // ties by lower index: the need-th smallest index among the entries equal to T
+    // (rare: scores exactly equal to the K-th)
+#pragma unroll
+    for (int r = 0; r < kTopkRanks; ++r)
+      for (int i = tid; i < sm.n_cand[r]; i += NT) {
+        const uint2 ci = sm.cand[r][i];
+        if (ci.x != T) continue;
+        int smaller = 0;
+        for (int r2 = 0; r2 < kTopkRanks; ++r2)
+          for (int i2 = 0; i2 < sm.n_cand[r2]; ++i2) {
+            const uint2 c2 = sm.cand[r2][i2];
+            smaller += c2.x == T && (int)c2.y < (int)ci.y;
+          }
+        if (smaller == need - 1) sm.tie_idx = (int)ci.y;
+      }
+    __syncthreads();
+  }
+  const int tie_idx = sm.tie_idx;   // 0x7FFFFFFF when every tie is taken
+  {
+    // selected candidates of the ranks before this one
+    int before = 0;
+    for (int r = 0; r < (int)rank; ++r)
+      for (int i = tid; i < sm.n_cand[r]; i += NT) {
+        const uint2 ci = sm.cand[r][i];
+        before += ci.x > T || (ci.x == T && (int)ci.y <= tie_idx);
+      }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (lane == 0 && before) atomicAdd(&sm.off, before);
+  }
+  __syncthreads();
+  const int off = sm.off;
+
+  // ---- this quarter's selection in index order
+  uint32_t sel = 0;
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    if (j0 + u < q1) {
+      const uint32_t key = order_key(x[u]);
+      if ((key >> 21) > (uint32_t)bstar || (((cm >> u) & 1u) && (key > T || (key == T && j0 + u <= tie_idx))))
+        sel |= 1u << u;
+    }
+  }
+  int p = off + block_exclusive_scan_t<NT>(__popc(sel), sm.warp_tot);
+  while (sel) {
+    const int u = __ffs(sel) - 1;
+    sel &= sel - 1;
+    if (p < kk) out[p] = remap_index(remap, row, j0 + u);
+    ++p;
+  }
 }
 
 // ---- many short rows (prefill: one row per query token) ------------------------------
@@ -1233,7 +1394,7 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(rows * kTopkRanks));
-    cfg.blockDim = dim3(kTopkThreads);
+    cfg.blockDim = dim3(kClThreads);
     cfg.dynamicSmemBytes = csm;
     cfg.stream = s;
     cudaLaunchAttribute at[2];

@@ -103,7 +103,7 @@ def _score_rows():
     # 11-bit key histogram, which takes the whole-row radix path
     for n, kind in [(40000, "normal"), (33333, "ties"), (5000, "ties2"), (512, "normal"), (300, "normal"),
                     (0, "normal"), (1, "normal"), (513, "zeros"), (20000, "neg"), (16385, "ties"),
-                    (40000, "const"), (30000, "narrow")]:
+                    (40000, "const"), (30000, "narrow"), (32768, "tiesK"), (32768, "tiesK2")]:
         if kind == "normal":
             r = torch.randn(stride, generator=g)
         elif kind == "ties":
@@ -118,6 +118,13 @@ def _score_rows():
             r = torch.full((stride,), 2.5)
         elif kind == "narrow":
             r = 1.0 + torch.rand(stride, generator=g) * 0.2
+        elif kind.startswith("tiesK"):
+            # 300 copies of the 401st (1,901st) largest value spread over the row: the
+            # Top-512 (Top-2048) takes some of the ties, by lower index
+            r = torch.randn(stride, generator=g)
+            v = torch.sort(r[:n], descending=True).values[400 if kind == "tiesK" else 1900]
+            below = torch.nonzero(r[:n] < v).flatten()
+            r[below[torch.randperm(len(below), generator=g)[:300]]] = v
         else:
             r = -torch.rand(stride, generator=g) * 1e-30 - 1e-38
         r[n:] = float("nan")   # never read: beyond the valid count
