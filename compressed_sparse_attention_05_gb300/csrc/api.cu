@@ -606,9 +606,9 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
   if (!reindex) {
     // the many-query GEMM path builds no histogram: the Top-K kernel then builds each row's
     if (index_scores_gemm_supported(a)) hist = nullptr;
-    if (hist) LAUNCH(cudaMemsetAsync(hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
+    if (hist) LAUNCH(launch_zero_u32(hist, rows * kHistBins, s), "zero histogram");
     if (!hist) bm_hist = nullptr;
-    if (bm_hist) LAUNCH(cudaMemsetAsync(bm_hist, 0, (size_t)rows * kHistBins * sizeof(uint32_t), s), "zero histogram");
+    if (bm_hist) LAUNCH(launch_zero_u32(bm_hist, rows * kHistBins, s), "zero histogram");
     bool bm_built = false;
     LAUNCH(launch_index_scores(a, scores, L.s_stride, out_pool ? bm : nullptr, L.bm_stride, 8, max_entries, hist, s,
                                bm_hist, &bm_built),

@@ -11,6 +11,8 @@
 // rows with 16-byte loads: the head dimension is visited in a permuted order
 // (the same permutation for q and k, so the dot products are unchanged) that
 // makes every warp load instruction touch 16 full 32-byte sectors.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc.cuh"
@@ -431,6 +433,23 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
       if (c) atomicAdd(&bm_hist[((int64_t)b * a.Tq + i0) * kHistBins + i], c);
     }
   }
+}
+
+// Zeroes a histogram buffer as a step kernel (a memset node would end the chain of
+// programmatic launches: the scan's prologue could not overlap it).
+__global__ void k_zero_u32x4(uint4* __restrict__ p, int64_t n4) {
+  pdl_trigger();
+  pdl_wait();   // an earlier kernel may still read the buffer
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+
+cudaError_t launch_zero_u32(uint32_t* p, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if ((reinterpret_cast<uintptr_t>(p) & 15) != 0 || n % 4 != 0) return cudaMemsetAsync(p, 0, (size_t)n * 4, s);
+  const int64_t n4 = n / 4;
+  const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, 1024);
+  return launch_step(k_zero_u32x4, dim3((unsigned)blocks), dim3(256), 0, s, reinterpret_cast<uint4*>(p), n4);
 }
 
 static int num_sms() {

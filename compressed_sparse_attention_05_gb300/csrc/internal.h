@@ -47,6 +47,9 @@ cudaError_t launch_step(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t 
   return counted(cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...));
 }
 
+// Zeroes n uint32 (a step kernel; falls back to a memset for unaligned buffers).
+cudaError_t launch_zero_u32(uint32_t* p, int64_t n, cudaStream_t s);
+
 // ---- pack.cu ----------------------------------------------------------------
 cudaError_t launch_pack_mxfp4(const float* x, int64_t n_rows, int d, uint8_t* codes,
                               uint8_t* scales, cudaStream_t s);
