@@ -698,12 +698,16 @@ def cpu_worker(workload, seconds, ref_steps=0, part=0):
                         wl.replay_hidden_rows(l, b)[i:i + 1].double().numpy()) for l in range(L)]
         else:
             win_lat = [wl.swa_latent(l, b, torch.from_numpy(win_pos)).numpy() for l in range(L)]
-        # cached state: packed rows of every entry the schedule can gather (the Full
-        # selection and, for the pooled indexer, every pooled position)
-        sc = I.index_scores(qs[0][0], qs[0][1], Kall[:nv])
-        cand = [I.topk(sc, wl.K)]
-        if wl.hierarchical:
-            cand.append(I.pool_positions(I.block_pool(sc, wl.pool_blocks, wl.pool_block), nv, wl.pool_block))
+        # cached state: packed rows of every entry the schedule can gather (each Full
+        # layer's selection and, for the pooled indexer, every pooled position)
+        cand = []
+        for l in range(L):
+            if wl.layers[l] != "F":
+                continue
+            sc = I.index_scores(qs[l][0], qs[l][1], Kall[:nv])
+            cand.append(I.topk(sc, wl.K))
+            if wl.hierarchical:
+                cand.append(I.pool_positions(I.block_pool(sc, wl.pool_blocks, wl.pool_block), nv, wl.pool_block))
         cand = np.unique(np.concatenate(cand))
         c, s = st.packed_rows(cand)
         prepared.append((t, nv, qs, Qs, win_lat, cand, c, s))
@@ -723,7 +727,8 @@ def cpu_worker(workload, seconds, ref_steps=0, part=0):
             idx = state["prev"]
         state["prev"] = idx
         rows = np.searchsorted(cand, idx)
-        kv = F.mxfp4_unpack(c[rows], s[rows])
+        assert np.array_equal(cand[rows], idx), "a gathered entry was not prepared"
+        kv = F.fp8_unpack_bf16(c[rows], s[rows]) if st.kv_format == "fp8" else F.mxfp4_unpack(c[rows], s[rows])
         if replay:
             wc, ws, own_h = win_lat[l]
             own = R.window_rows(own_h, W_swa[l], st.gamma, wl.eps, wl.r, wl.rope_base, t)
