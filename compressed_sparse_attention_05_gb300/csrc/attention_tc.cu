@@ -218,31 +218,55 @@ __device__ __forceinline__ bool workers_or(bool v) {
   return r != 0;
 }
 
-// Packed MXFP4 code bytes of one key for the thread's 32 dims (128*sl +
-// 32*qd ..) of each slice sl, in v[sl], so that a slice's registers can be
-// refilled with the next chunk's bytes as soon as the slice is stored.
-// (Window rows, one chunk per token at most, are read when they are stored.)
+// Packed bytes of one key for the thread's 32 dims (128*sl + 32*qd ..) of each
+// slice sl, held in registers from the moment they are requested until the slice
+// is stored, so that the gather of the next chunk overlaps this chunk's products.
 struct KeyBytes {
   uint4 v[4];
 };
+// Loads that the compiler keeps where they are written (volatile): a plain load
+// may be moved down to its first use, which would turn the prefetch into a stall.
+__device__ __forceinline__ uint4 ld_gather16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_gather8(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_gather4f(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
 // MXFP4 scales of a key: quarter qd loads bytes 8*qd .. +7 (the groups of slice qd)
 __device__ __forceinline__ uint2 load_scales(const AttnArgs& a, int32_t src, int qd) {
-  return src >= 0 ? __ldg(reinterpret_cast<const uint2*>(a.kv_scales + (int64_t)src * (kD / 16) + 8 * qd))
-                  : make_uint2(0, 0);
+  return src >= 0 ? ld_gather8(a.kv_scales + (int64_t)src * (kD / 16) + 8 * qd) : make_uint2(0, 0);
+}
+// A key stored as an FP8 row: a window row, or a main-KV entry in the FP8 format.
+template <bool kFp8>
+__device__ __forceinline__ bool fp8_row_key(int32_t src) {
+  return src <= -2 || (kFp8 && src >= 0);
 }
 
-// Packed bytes of slice SL of a main-KV key for the thread's 32 dims.  MXFP4:
-// 16 bytes, in v[SL].  FP8 rows: 32 bytes, in v[2 (SL & 1)] and the next (slices
-// 0 and 1 are prefetched together, slices 2 and 3 reuse their registers).
+// Packed bytes of slice SL of a key for the thread's 32 dims.  MXFP4 entry:
+// 16 bytes, in v[SL] (all four slices are requested together).  FP8 row: 32
+// bytes, in v[2 (SL & 1)] and the next (slices 0 and 1 are requested together,
+// slices 2 and 3 reuse their registers once 0 and 1 are stored).
 template <int SL, bool kFp8>
 __device__ __forceinline__ void load_slice(const AttnArgs& a, int32_t src, int qd, KeyBytes& kb) {
-  if (src < 0) return;
-  if (kFp8) {
-    const uint8_t* p = a.kv_codes + (int64_t)src * kD + 32 * qd + 128 * SL;
-    kb.v[2 * (SL & 1)] = __ldg(reinterpret_cast<const uint4*>(p));
-    kb.v[2 * (SL & 1) + 1] = __ldg(reinterpret_cast<const uint4*>(p + 16));
+  if (src == -1) return;
+  if (fp8_row_key<kFp8>(src)) {
+    const uint8_t* p = (src <= -2 ? a.swa_codes + (-2 - (int64_t)src) * kD : a.kv_codes + (int64_t)src * kD) +
+                       32 * qd + 128 * SL;
+    kb.v[2 * (SL & 1)] = ld_gather16(p);
+    kb.v[2 * (SL & 1) + 1] = ld_gather16(p + 16);
   } else {
-    kb.v[SL] = __ldg(reinterpret_cast<const uint4*>(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL));
+    kb.v[SL] = ld_gather16(a.kv_codes + (int64_t)src * (kD / 2) + 16 * qd + 64 * SL);
   }
 }
 // Dequantisation scale of an FP8 row (a window row, or a main-KV entry in the FP8
@@ -250,8 +274,8 @@ __device__ __forceinline__ void load_slice(const AttnArgs& a, int32_t src, int q
 template <bool kFp8>
 __device__ __forceinline__ float load_wscale(const AttnArgs& a, int32_t src) {
   float sw;
-  if (src <= -2) sw = __ldg(a.swa_scales + (-2 - (int64_t)src));
-  else if (kFp8 && src >= 0) sw = __ldg(reinterpret_cast<const float*>(a.kv_scales) + src);
+  if (src <= -2) sw = ld_gather4f(a.swa_scales + (-2 - (int64_t)src));
+  else if (kFp8 && src >= 0) sw = ld_gather4f(reinterpret_cast<const float*>(a.kv_scales) + src);
   else return 0.f;
   return sw * pow2i(-window_exp(sw));
 }
@@ -284,7 +308,7 @@ template <int SL, bool kFp8>
 __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& kb, uint32_t sc_pair, int32_t src,
                                             float wsc, int key, int qd, unsigned char* ktile) {
   unsigned char* dst = ktile + (key >> 3) * 8192 + (16 * SL + 4 * qd) * 128 + (key & 7) * 16;
-  if (src >= 0 && kFp8) {
+  if (fp8_row_key<kFp8>(src)) {
     store_fp8_dims(kb.v[2 * (SL & 1)], kb.v[2 * (SL & 1) + 1], wsc, dst);
   } else if (src >= 0) {
     const uint32_t s = e4m3x2_f16x2(sc_pair);
@@ -300,9 +324,6 @@ __device__ __forceinline__ void store_slice(const AttnArgs& a, const KeyBytes& k
       o.w = hmul2(e2m1x2_f16x2(w >> 24), s2);
       *reinterpret_cast<uint4*>(dst + j * 128) = o;
     }
-  } else if (src <= -2) {
-    const uint8_t* wc = a.swa_codes + (-2 - (int64_t)src) * kD + 32 * qd + 128 * SL;
-    store_fp8_dims(__ldg(reinterpret_cast<const uint4*>(wc)), __ldg(reinterpret_cast<const uint4*>(wc + 16)), wsc, dst);
   } else {
 #pragma unroll
     for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(dst + j * 128) = make_uint4(0, 0, 0, 0);
@@ -515,7 +536,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
   if (!mma_warp && n_my > 0) {
     load_slice<0, kFp8>(a, cur_src, qd, kb);
     load_slice<1, kFp8>(a, cur_src, qd, kb);
-    if (!kFp8) {
+    if (!fp8_row_key<kFp8>(cur_src)) {
       load_slice<2, kFp8>(a, cur_src, qd, kb);
       load_slice<3, kFp8>(a, cur_src, qd, kb);
       cur_sc = load_scales(a, cur_src, qd);
@@ -587,7 +608,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       const uint32_t pr = ((qd >> 1) ? w1 : w0) >> (16 * (qd & 1));                      \
       if (wok) store_slice<SL, kFp8>(a, kb, pr & 0xFFFFu, cur_src, cur_wsc, key, qd, ktile); \
       /* FP8 rows: slices 2 and 3 of this chunk reuse the registers of 0 and 1 */        \
-      if (kFp8 && SL < 2) load_slice<(SL + 2) & 3, kFp8>(a, cur_src, qd, kb);            \
+      if (SL < 2 && fp8_row_key<kFp8>(cur_src)) load_slice<(SL + 2) & 3, kFp8>(a, cur_src, qd, kb); \
     }                                                                                    \
     tc::fence_async_smem();                                                              \
     __syncwarp();                                                                        \
@@ -602,7 +623,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
       if (it + 1 < n_my) {
         load_slice<0, kFp8>(a, nxt_src, qd, kb);
         load_slice<1, kFp8>(a, nxt_src, qd, kb);
-        if (!kFp8) {
+        if (!fp8_row_key<kFp8>(nxt_src)) {
           load_slice<2, kFp8>(a, nxt_src, qd, kb);
           load_slice<3, kFp8>(a, nxt_src, qd, kb);
         }
