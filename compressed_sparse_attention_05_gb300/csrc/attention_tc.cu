@@ -735,7 +735,7 @@ k_sparse_attn_tc(AttnArgs a, uint32_t* status, int n_split) {
 
   if (n_split == 1) {
     if (tid < kHeads) sm.fac[tid] = sm.l_run[tid] > 0.f ? 1.f / sm.l_run[tid] : 0.f;
-    if (a.lse && hb + tid < a.Hq) {
+    if (a.lse && tid < kHeads && hb + tid < a.Hq) {
       const float l = sm.l_run[tid];
       a.lse[row * a.Hq + hb + tid] = l > 0.f ? (sm.m_ref[tid] + log2f(l)) * 0.6931471805599453f : -INFINITY;
     }

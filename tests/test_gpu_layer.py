@@ -68,6 +68,26 @@ def test_prefill_small_with_compression_fp8kv():
     check_compressed_entries(g, wl, 0)
 
 
+@pytest.mark.parametrize("Hq", [128, 40])
+def test_decode_small_head_groups(Hq):
+    """Hq = 128: two groups of 64 heads (blockIdx.y), each merged over its own
+    cluster; Hq = 40: one group with 24 zero-padded heads."""
+    wl = _decode_small()
+    wl.Hq = Hq
+    wl.name = f"decode_small_hq{Hq}"
+    check_group(wl, [(0, 0), (1, 0), (2, 0)])
+
+
+def test_prefill_small_hq96():
+    """One CTA per token (256 rows), 96 heads: a full group of 64 and a partial
+    group of 32; every head's output and lse written by its own group only."""
+    wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
+    wl.Hq = 96
+    wl.name = "prefill_small_hq96"
+    g, _ = check_group(wl, [(0, i) for i in (0, 1, 100, 255)])
+    assert torch.isfinite(g.lse[0]).all() and torch.isfinite(g.O[0]).all()   # every row and head written
+
+
 def test_prefill_small_with_compression():
     wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
     g, _ = check_group(wl, [(0, i) for i in (0, 1, 2, 3, 4, 100, 254, 255)])
