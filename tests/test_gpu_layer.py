@@ -68,6 +68,24 @@ def test_prefill_small_with_compression_fp8kv():
     check_compressed_entries(g, wl, 0)
 
 
+def test_decode_small_max_keys():
+    """The largest key list the header admits: Top-2048 plus a 1,024-row window
+    (24 chunks of 128 keys) spread over a cluster of 8 CTAs."""
+    wl = _decode_small()
+    wl.K, wl.W = 2048, 1024
+    wl.name = "decode_small_max_keys"
+    check_group(wl, [(0, 0), (1, 0), (2, 0)])
+
+
+def test_prefill_small_max_keys():
+    """One CTA per token over up to 17 chunks: every visible entry (Top-2048 of
+    at most 1,088) plus a 1,024-row window."""
+    wl = WL.prefill_64k(n_new=256, ctx=4096 + 256, H=256)
+    wl.K, wl.W = 2048, 1024
+    wl.name = "prefill_small_max_keys"
+    check_group(wl, [(0, i) for i in (0, 1, 128, 255)])
+
+
 @pytest.mark.parametrize("Hq", [128, 40])
 def test_decode_small_head_groups(Hq):
     """Hq = 128: two groups of 64 heads (blockIdx.y), each merged over its own
