@@ -218,8 +218,9 @@ def test_index_scores_many_queries():
 # ---- full-size workloads, sampled ------------------------------------------------------
 
 def test_full_decode_128k_b32():
+    """The bench's decode launch, 8 of its 32 tokens spread over the batch."""
     wl = WL.decode_128k()
-    check_group(wl, [(0, 0), (31, 0)])
+    check_group(wl, [(b, 0) for b in (0, 3, 7, 12, 18, 24, 29, 31)])
 
 
 def test_full_decode_fp8kv_128k_b32():
@@ -229,7 +230,7 @@ def test_full_decode_fp8kv_128k_b32():
 
 def test_full_hierarchical_1m_b8():
     wl = WL.hierarchical_1m()
-    check_group(wl, [(5, 0)])
+    check_group(wl, [(0, 0), (5, 0), (7, 0)])
 
 
 def test_full_ragged_b64():
