@@ -1094,12 +1094,14 @@ k_topk_short(const float* __restrict__ scores, int64_t stride, ValidSpec v, int 
     __syncthreads();
   }
 
-  // ---- one pass: entries at or above the bound -> candidates and their histogram
-  collect_batch<kVec>(sm, x0, 0, n, take_all, f_lo, tid);
-  for (int j0 = kStep; j0 < n; j0 += kStep) {
-    float x[kShortBatch];
-    load_batch<kVec>(s, n, j0, tid, x);
-    collect_batch<kVec>(sm, x, j0, n, take_all, f_lo, tid);
+  // ---- one pass: entries at or above the bound -> candidates and their histogram;
+  // the next batch is requested before the current one is collected
+  for (int j0 = 0; j0 < n; j0 += kStep) {
+    float x1[kShortBatch];
+    if (j0 + kStep < n) load_batch<kVec>(s, n, j0 + kStep, tid, x1);
+    collect_batch<kVec>(sm, x0, j0, n, take_all, f_lo, tid);
+#pragma unroll
+    for (int u = 0; u < kShortBatch; ++u) x0[u] = x1[u];
   }
   __syncthreads();
   const int nC = sm.nC;
