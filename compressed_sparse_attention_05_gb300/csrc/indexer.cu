@@ -273,7 +273,6 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
   extern __shared__ __align__(128) unsigned char smem_raw[];
   __shared__ ScanShared ss;
   pdl_trigger();
-  pdl_wait();
   unsigned char* ring = smem_raw;                                   // kScanStages pages
   uint32_t* shist = reinterpret_cast<uint32_t*>(smem_raw + kScanStages * kPageBytes);
   // block-maxima histogram of the (one) query row, after the score histogram
@@ -310,6 +309,9 @@ k_index_scan_pages(IndexerArgs a, int QG, int pages_per_cta, int flat_slots, flo
   if (bm_hist)   // one query row per CTA on this path (checked by the launcher)
     for (int i = threadIdx.x; i < kHistBins; i += blockDim.x) sbm[i] = 0;
   __syncthreads();
+  // The set-up above reads inputs only (counts, positions); the keys (new entries
+  // of a compressing step), the scores and the histograms belong to earlier kernels.
+  pdl_wait();
   volatile int* abort = &ss.abort;
 
   if (warp == kScanConsumers) {
