@@ -38,6 +38,13 @@ FLUSH_BYTES = 512 << 20
 # ---------------------------------------------------------------------------------
 # workload bytes / flops (algorithmic: what the method must move or compute)
 
+def workload_config(wl):
+    """The workload's shape keys of the JSON line's config (the same in both arms)."""
+    return {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": wl.B * wl.Tq,
+            "layers": "".join(wl.layers), "K": wl.K, "Hq": wl.Hq, "d": wl.d, "W": wl.W,
+            "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": kv_desc(wl)}
+
+
 def kv_desc(wl):
     if getattr(wl, "kv_format", "mxfp4") == "fp8":
         return f"FP8 E4M3 + fp32 scale, {wl.d + 4} B/entry, 64-entry pages"
@@ -289,11 +296,9 @@ def measure(args, workload, steps, rank, world, dist, local):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "B": wl.B, "tokens_per_step": tokens,
-                   "layers": "".join(wl.layers), "K": wl.K, "Hq": wl.Hq, "d": wl.d, "W": wl.W,
-                   "indexer": f"{wl.Hi}x{wl.Di} {wl.idx_dtype}", "kv": kv_desc(wl),
-                   "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": dict(workload_config(wl),
+                       l2="flushed before every timed step (512 MB written, then 512 MB read)",
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
         "roofline": roof,
         "step_roofline": step_roofline(wl, alg, ms, peaks),
         "e2e": e2e,
@@ -828,7 +833,9 @@ def run_reference(args, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": ({"workload": f"ced_compress_{CED_LAYERS}layers_chunk{wl.n_new}",
                     "description": f"{CED_LAYERS} layers' KV of a {wl.n_new}-token chunk from one hidden state"}
-                   if args.workload == "ced_compress" else {"workload": wl.name, "description": wl.description}),
+                   if args.workload == "ced_compress"
+                   else dict(workload_config(wl), l2="not applicable (host cores)",
+                             parallelism="one single-threaded host process")),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": last["cores"], "kind": "oracle",
                          "sample": last["sample"]},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
