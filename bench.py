@@ -539,37 +539,63 @@ def time_replay(args, g, wl, flush, stream):
 
 
 def time_e2e(args, g, flush, stream, dist):
-    """Same step through the public call, per-step inputs copied from pinned host memory
-    before it and the attention outputs read back after it, all inside the timed region."""
+    """The metric end to end through the public call (csa2_layer) with host buffers,
+    as a serving loop runs it: two sets of device input/output buffers (a second
+    layer group over an identical cache), a copy stream that uploads step i+1's
+    inputs from pinned host memory and downloads step i-1's outputs while step i
+    computes.  Every step's inputs are copied in and its outputs copied out inside
+    the timed region, which runs from the first upload to the last download.  No
+    L2 flush between steps: each step streams more than L2 (its keys and cache)."""
     import torch
 
-    ins = g.step_inputs()
-    outs = g.step_outputs()
-    h_in = [t.detach().cpu().pin_memory() for t in ins]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    bi = sum(t.numel() * t.element_size() for t in ins)
-    bo = sum(t.numel() * t.element_size() for t in outs)
-    n = max(3, min(args.steps, 200))
-    tot = 0.0
+    from compressed_sparse_attention_05_gb300 import harness
+
+    g2 = harness.LayerGroup(g.wl, g.Q[0].device)
+    groups = [g, g2]
+    ins = [x.step_inputs() for x in groups]
+    outs = [x.step_outputs() for x in groups]
+    h_in = [t.detach().cpu().pin_memory() for t in ins[0]]
+    h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs[0]] for _ in range(2)]
+    bi = sum(t.numel() * t.element_size() for t in ins[0])
+    bo = sum(t.numel() * t.element_size() for t in outs[0])
+    cs = torch.cuda.Stream(device=g.Q[0].device)
+    n = max(4, min(args.steps, 200))
+
+    def run(n_steps):
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(cs)
+        for i in range(n_steps + 2):
+            j = i % 2
+            with torch.cuda.stream(cs):
+                if i >= 2:   # buffer set j: step i-2 has finished; its outputs go to the host
+                    cs.wait_event(done[j])
+                    for h, d_ in zip(h_out[j], outs[j]):
+                        h.copy_(d_, non_blocking=True)
+                if i < n_steps:   # step i's inputs
+                    for d_, h in zip(ins[j], h_in):
+                        d_.copy_(h, non_blocking=True)
+                    up[j].record(cs)
+            if i < n_steps:
+                stream.wait_event(up[j])
+                groups[j].step(stream=stream)
+                done[j].record(stream)
+        end.record(cs)
+        end.synchronize()
+        return start.elapsed_time(end)
+
+    run(4)   # warm-up
     if dist is not None:
         dist.barrier()
-    for k in range(n):
-        flush(k)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for d_, h in zip(ins, h_in):
-            d_.copy_(h, non_blocking=True)
-        g.step()
-        for h, d_ in zip(h_out, outs):
-            h.copy_(d_, non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        tot += a.elapsed_time(b)
-    ms = max_over_ranks(tot / n, dist, flush.device)
+    ms = max_over_ranks(run(n) / n, dist, flush.device)
     world = dist.get_world_size() if dist is not None else 1
     wl = g.wl
+    del g2
     return {"value": world * wl.B * wl.Tq / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "pipeline": "two buffer sets; uploads and downloads on a copy stream overlap the steps' compute; "
+                        "no L2 flush (each step streams more than L2)"}
 
 
 def load_peaks():
