@@ -23,8 +23,11 @@ def _np(t):
     return t.detach().cpu().double().numpy()
 
 
-@pytest.mark.parametrize("d,r,Di,idx_dtype", [(512, 64, 128, "bf16"), (512, 64, 0, "bf16"), (64, 16, 32, "f32")])
-def test_compress_layers_matches_oracle(d, r, Di, idx_dtype):
+@pytest.mark.parametrize("d,r,Di,idx_dtype,kv", [(512, 64, 128, "bf16", "mxfp4"), (512, 64, 0, "bf16", "mxfp4"),
+                                                (64, 16, 32, "f32", "mxfp4"), (512, 64, 128, "bf16", "fp8")])
+def test_compress_layers_matches_oracle(d, r, Di, idx_dtype, kv):
+    """kv = "fp8": the V4-style main KV (E4M3 row + fp32 scale per entry)."""
+    fp8 = kv == "fp8"
     dev = "cuda"
     g = torch.Generator().manual_seed(21)
     B, H, L = 2, 256, 3
@@ -41,8 +44,9 @@ def test_compress_layers_matches_oracle(d, r, Di, idx_dtype):
     caches, keep = [], []
     for l in range(L):
         perm = torch.randperm(n_pages, generator=g).to(torch.int32).reshape(B, pages)
-        t = {"codes": torch.zeros(n_pages * 64, d // 2, dtype=torch.uint8, device=dev),
-             "scales": torch.zeros(n_pages * 64, d // 16, dtype=torch.uint8, device=dev),
+        t = {"codes": torch.zeros(n_pages * 64, d if fp8 else d // 2, dtype=torch.uint8, device=dev),
+             "scales": (torch.zeros(n_pages * 64, dtype=torch.float32, device=dev) if fp8
+                        else torch.zeros(n_pages * 64, d // 16, dtype=torch.uint8, device=dev)),
              "idx": torch.zeros(n_pages * 64, max(Di, 1), dtype=idx_t, device=dev),
              "pt": perm.to(dev), "n": torch.tensor([f + G for f in first], dtype=torch.int32, device=dev)}
         keep.append(t)
@@ -51,7 +55,8 @@ def test_compress_layers_matches_oracle(d, r, Di, idx_dtype):
                                 n_entries=t["n"].data_ptr(), n_pages=n_pages))
     dims = abi.Dims(B=B, Tq=T, d=d, r=r, Hq=4, Hi=4, Di=Di if Di else 32,
                     idx_dtype=abi.CSA2_BF16 if idx_dtype == "bf16" else abi.CSA2_F32, K=16, W=16,
-                    max_pages=pages, n_pool_blocks=0, pool_block=8, swa_cap=0)
+                    max_pages=pages, n_pool_blocks=0, pool_block=8, swa_cap=0,
+                    kv_format=abi.CSA2_KV_FP8 if fp8 else abi.CSA2_KV_MXFP4)
     ws = torch.empty(max(256, abi.csa2_compress_layers_workspace_size(B, T, H, L, d, Di)), dtype=torch.uint8,
                      device=dev)
     fe = torch.tensor(first, dtype=torch.int32, device=dev)
@@ -63,7 +68,7 @@ def test_compress_layers_matches_oracle(d, r, Di, idx_dtype):
         Wi = _np(W_all[l, d:]) if Di else None
         for b in range(B):
             ref = Cm.compress_pack(_np(hidden[b]), W, _np(gamma[l]), eps, r, base, first[b], W_idx=Wi,
-                                   idx_dtype=idx_dtype)
+                                   idx_dtype=idx_dtype, kv_format=kv)
             ids = torch.from_numpy(ref["entry_ids"])
             assert len(ids) == G
             slots = keep[l]["pt"][b, ids // 64].long().cpu() * 64 + ids % 64
@@ -73,7 +78,10 @@ def test_compress_layers_matches_oracle(d, r, Di, idx_dtype):
             cat = Cm.concat_groups(_np(hidden[b]))
             tau_x = parity.latent_error_bound(ref["c"], parity.gemm_error_bound(cat, W), _np(gamma[l]), eps, r,
                                               ref["x"])
-            parity.check_mxfp4_after_gemm(codes, scales, ref["x"], tau_x)
+            if fp8:
+                parity.check_fp8_after_gemm(codes, scales, ref["x"], tau_x)
+            else:
+                parity.check_mxfp4_after_gemm(codes, scales, ref["x"], tau_x)
             if Di:
                 kk = keep[l]["idx"][slots.to(dev)].float().cpu().double().numpy()
                 parity.check_keys_after_gemm(kk, cat @ Wi.T, parity.gemm_error_bound(cat, Wi), idx_dtype)
