@@ -214,9 +214,9 @@ def test_topk_bit_exact_with_histogram(stride, k):
 
 def _many_short_rows(stride):
     """320 rows (more than twice the SM count) of at most 32,768 entries: the
-    four-rows-per-SM path (sampled lower bound, candidates only; the whole-row
+    many-short-rows path (sampled lower bound, candidates only; the whole-row
     radix fallback for rows of equal or crowded scores), vectorised when rows
-    are 16-byte aligned."""
+    are 16-byte aligned (strides 16,384, 4,000 and 32,768)."""
     g = torch.Generator().manual_seed(16)
     kinds = ["normal", "ties", "ties2", "zeros", "neg", "const", "narrow", "normal"]
     rows, n_valid = [], []
@@ -245,7 +245,7 @@ def _many_short_rows(stride):
     return torch.stack(rows).contiguous(), torch.tensor(n_valid, dtype=torch.int32)
 
 
-@pytest.mark.parametrize("stride", [16384, 12001, 32768])
+@pytest.mark.parametrize("stride", [16384, 4000, 12001, 32768])
 @pytest.mark.parametrize("k", [512, 7])
 def test_topk_bit_exact_many_short_rows(stride, k):
     s, nv = _many_short_rows(stride)
