@@ -159,6 +159,12 @@ k_compress_gemm(const uint16_t* __restrict__ hidden, int G, int T, int H, const 
 // accumulator in tensor memory, warps 2..5 write the fp32 partial sums.
 // Split K: grid.z = B x n_split, split s takes stages [s n / n_split,
 // (s + 1) n / n_split).  Every wait is bounded.
+//
+// kMc > 1: the kMc CTAs of a cluster take consecutive M tiles of the same N
+// tile; each copies 1/kMc of the B tile and multicasts it to all of them, so
+// that a CTA reads 16 KB + 32/kMc KB per stage from L2 instead of 48 KB.  A
+// stage is refilled only once every CTA of the cluster has released it (each
+// CTA's MMA commit arrives on the stage's empty barrier of all of them).
 constexpr int kTmM = 128, kTmN = 256, kTmK = 64, kTmStages = 4;
 constexpr int kTmABytes = kTmM * kTmK * 2;                 // 16 KB
 constexpr int kTmStageBytes = kTmABytes + kTmN * kTmK * 2;   // 48 KB
@@ -182,6 +188,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
   return false;
 }
 
+template <int kMc>
 __global__ void __launch_bounds__(kTmThreads, 1)
 k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap wmap,
                     const __grid_constant__ CUtensorMap imap, int G, int d, int Di, int N, int M, int n_stages,
@@ -200,7 +207,7 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
   if (tid == 0) {
     for (int i = 0; i < kTmStages; ++i) {
       tc::mbar_init(&sm.full[i], 1);
-      tc::mbar_init(&sm.empty[i], 1);
+      tc::mbar_init(&sm.empty[i], kMc);
     }
     tc::mbar_init(&sm.acc_full, 1);
     sm.abort = 0;
@@ -210,6 +217,10 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  if (kMc > 1) tc::cluster_barrier();   // every CTA's barriers exist before a peer copies or arrives into them
+  const uint32_t crank = kMc > 1 ? tc::cluster_ctarank() : 0;
+  constexpr uint16_t kMask = (uint16_t)((1u << kMc) - 1);
+  constexpr int kBRows = kTmN / kMc;   // B rows this CTA copies (kMc > 1)
   const uint32_t tm = sm.tmem;
   volatile int* abort = &sm.abort;
 
@@ -220,11 +231,24 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
       for (int i = 0; i < my; ++i) {
         const int st = i % kTmStages;
         if (i >= kTmStages && !wait_or_abort(&sm.empty[st], ((i / kTmStages) - 1) & 1, abort)) break;
-        tc::mbar_arrive_expect_tx(&sm.full[st], (uint32_t)(kTmABytes + (n0 < d ? kTmN : Di) * kTmK * 2));
         const int kx = (s0 + i) * kTmK;
-        tma::load_3d(sm.ring[st], &amap, kx, j0, b, &sm.full[st]);
-        if (n0 < d) tma::load_2d(sm.ring[st] + kTmABytes, &wmap, kx, n0, &sm.full[st]);
-        else tma::load_2d(sm.ring[st] + kTmABytes, &imap, kx, n0 - d, &sm.full[st]);
+        if (kMc > 1) {
+          // the B tile's rows held by W (or W_idx) in parts of kBRows; the parts past them are not copied
+          const int rows = n0 < d ? min(kTmN, d - n0) : Di;
+          const int parts = (rows + kBRows - 1) / kBRows;
+          tc::mbar_arrive_expect_tx(&sm.full[st], (uint32_t)(kTmABytes + parts * kBRows * kTmK * 2));
+          tma::load_3d(sm.ring[st], &amap, kx, j0, b, &sm.full[st]);
+          if ((int)crank < parts) {
+            unsigned char* bdst = sm.ring[st] + kTmABytes + crank * (kBRows * kTmK * 2);
+            if (n0 < d) tma::load_2d_mc(bdst, &wmap, kx, n0 + (int)crank * kBRows, &sm.full[st], kMask);
+            else tma::load_2d_mc(bdst, &imap, kx, n0 - d + (int)crank * kBRows, &sm.full[st], kMask);
+          }
+        } else {
+          tc::mbar_arrive_expect_tx(&sm.full[st], (uint32_t)(kTmABytes + (n0 < d ? kTmN : Di) * kTmK * 2));
+          tma::load_3d(sm.ring[st], &amap, kx, j0, b, &sm.full[st]);
+          if (n0 < d) tma::load_2d(sm.ring[st] + kTmABytes, &wmap, kx, n0, &sm.full[st]);
+          else tma::load_2d(sm.ring[st] + kTmABytes, &imap, kx, n0 - d, &sm.full[st]);
+        }
         issued = i + 1;
       }
       for (int i = max(0, issued - kTmStages); i < issued; ++i)   // every issued copy lands before exit
@@ -247,7 +271,8 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
           const uint64_t bd = tc::smem_desc(sb + ks * 32, 16, 1024) | ((uint64_t)2 << 61);
           tc::mma_f16(tm, ad, bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&sm.empty[st]);
+        if (kMc > 1) tc::mma_commit_mc(&sm.empty[st], kMask);   // the stage is free in this CTA
+        else tc::mma_commit(&sm.empty[st]);
       }
       tc::mma_commit(&sm.acc_full);   // arrives once every MMA issued above is complete
     }
@@ -275,6 +300,7 @@ k_compress_gemm_tma(const __grid_constant__ CUtensorMap amap, const __grid_const
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (kMc > 1) tc::cluster_barrier();   // no copy or commit of a peer still targets this CTA
   if (warp == 1) tc::tmem_dealloc(tm, kTmN);
   if (tid == 0 && *abort) raise_status(status, CSA2_STATUS_TIMEOUT);
 }
@@ -315,9 +341,12 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
     const cuuint32_t abox[3] = {kTmK, kTmM, 1};
     const cuuint64_t wdims[2] = {(cuuint64_t)Kd, (cuuint64_t)d};
     const cuuint64_t wstr[1] = {(cuuint64_t)Kd * 2};
-    const cuuint32_t wbox[2] = {kTmK, kTmN};
+    // clusters of mc CTAs along M share each B tile (each copies and multicasts 1/mc of it)
+    const int m_tiles = (G + kTmM - 1) / kTmM;
+    const int mc = m_tiles % 4 == 0 ? 4 : (m_tiles % 2 == 0 ? 2 : 1);
+    const cuuint32_t wbox[2] = {kTmK, (cuuint32_t)(kTmN / mc)};
     const cuuint64_t idims[2] = {(cuuint64_t)Kd, (cuuint64_t)(W_idx ? Di : d)};
-    const cuuint32_t ibox[2] = {kTmK, (cuuint32_t)(W_idx ? Di : kTmN)};
+    const cuuint32_t ibox[2] = {kTmK, (cuuint32_t)(mc > 1 ? kTmN / mc : (W_idx ? Di : kTmN))};
     EncodeTiled enc = tensor_map_encoder();
     if (enc(&amap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(hidden), adims, astr, abox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -330,11 +359,25 @@ cudaError_t launch_compress_gemm(const uint16_t* hidden, int B, int T, int H, co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
     const size_t smem = sizeof(CompressSmem) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(k_compress_gemm_tma, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    auto kernel = mc == 4 ? k_compress_gemm_tma<4> : (mc == 2 ? k_compress_gemm_tma<2> : k_compress_gemm_tma<1>);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((N + kTmN - 1) / kTmN, (G + kTmM - 1) / kTmM, B * n_split);
-    return launch_step(k_compress_gemm_tma, grid, dim3(kTmThreads), smem, s, amap, wmap, imap, G, d,
-                       W_idx ? Di : 0, N, M, Kd / kTmK, n_split, partials, status_word());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((N + kTmN - 1) / kTmN, m_tiles, B * n_split);
+    cfg.blockDim = dim3(kTmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = (unsigned)mc;
+    at[1].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = mc > 1 ? 2 : 1;
+    return counted(cudaLaunchKernelEx(&cfg, kernel, amap, wmap, imap, G, d, W_idx ? Di : 0, N, M, Kd / kTmK, n_split,
+                                      partials, status_word()));
   }
   dim3 grid((N + kGN - 1) / kGN, (M + kGM - 1) / kGM, n_split);
   k_compress_gemm<<<grid, kGThreads, 0, s>>>(hidden, G, T, H, W, d, W_idx, W_idx ? Di : 0, M, partials, g);

@@ -127,6 +127,23 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
+// mma_commit arriving on the barrier at `bar`'s offset in every CTA of the cluster in cta_mask.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                   "r"(smem_addr(bar)), "h"(cta_mask)
+               : "memory");
+}
+// Rank of the CTA in its cluster, and a barrier of all threads of the cluster
+// (release / acquire at cluster scope).
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 32 lanes x 16 columns of 32-bit: thread i of the warp gets lane (base + i),
 // columns col .. col+15.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {

@@ -47,5 +47,16 @@ __device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* map, int x
       : "memory");
 }
 
+// load_2d into the same shared-memory offset of every CTA of the cluster in cta_mask,
+// completing the transaction bytes on each destination CTA's barrier at `bar`'s offset.
+__device__ __forceinline__ void load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                           uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(tc::smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(tc::smem_addr(bar)), "h"(cta_mask)
+      : "memory");
+}
+
 }  // namespace tma
 }  // namespace csa2
