@@ -423,13 +423,20 @@ int csa2_compress_layers(const uint16_t* hidden, int32_t B, int32_t T, int32_t H
   compress_partials_bytes(B, T, H, N, 0, &n_split);
   float* part = static_cast<float*>(ws);
   LAUNCH(launch_compress_gemm(hidden, B, T, H, W_all, N, nullptr, 0, part, n_split, s), "compress_layers_gemm");
-  for (int l = 0; l < L; ++l) {
-    const csa2_cache* c = &caches[l];
-    LatentSource src{part + (int64_t)l * Nl, N, (int64_t)B * G * N, n_split};
-    LAUNCH(launch_norm_rope_pack(src, B, G, d, dm->r, gamma_all + (int64_t)l * d, eps, rope_base, first_entry,
-                                 nullptr, c->page_table, dm->max_pages, c->n_pages, c->kv_codes, c->kv_scales,
-                                 Di ? part + (int64_t)l * Nl + d : nullptr, N, Di, dm->idx_dtype,
-                                 Di ? c->idx_k : nullptr, s, dm->kv_format == CSA2_KV_FP8),
+  // every layer's RMSNorm / RoPE / pack in one launch per kPackLayersMax layers
+  for (int l0 = 0; l0 < L; l0 += kPackLayersMax) {
+    const int nl = std::min(L - l0, kPackLayersMax);
+    PackLayers pl = {};
+    pl.col_stride = Nl;
+    pl.gamma_stride = d;
+    for (int l = 0; l < nl; ++l) {
+      const csa2_cache* c = &caches[l0 + l];
+      pl.l[l] = PackLayer{c->page_table, c->n_pages, c->kv_codes, c->kv_scales, Di ? c->idx_k : nullptr};
+    }
+    LatentSource src{part + (int64_t)l0 * Nl, N, (int64_t)B * G * N, n_split};
+    LAUNCH(launch_norm_rope_pack_layers(src, B, G, d, dm->r, gamma_all + (int64_t)l0 * d, eps, rope_base,
+                                        first_entry, dm->max_pages, Di ? part + (int64_t)l0 * Nl + d : nullptr, N, Di,
+                                        dm->idx_dtype, dm->kv_format == CSA2_KV_FP8, pl, nl, s),
            "compress_layers_epilogue");
   }
   return CSA2_OK;

@@ -71,6 +71,24 @@ struct LatentSource {
   int64_t split_stride;  // elements between split-K partials (0: one split)
   int n_split;
 };
+// Per-layer caches of launch_norm_rope_pack_layers (at most kPackLayersMax layers per launch).
+constexpr int kPackLayersMax = 64;
+struct PackLayer {
+  const int32_t* page_table;
+  int64_t n_pages;
+  uint8_t* kv_codes;
+  uint8_t* kv_scales;
+  void* idx_k;
+};
+struct PackLayers {
+  int64_t col_stride;     // GEMM output columns between consecutive layers
+  int64_t gamma_stride;   // gamma elements between consecutive layers
+  PackLayer l[kPackLayersMax];
+};
+cudaError_t launch_norm_rope_pack_layers(LatentSource src, int B, int n_max, int d, int r, const float* gamma,
+                                         float eps, float rope_base, const int32_t* first_entry, int max_pages,
+                                         const float* idx_src, int64_t idx_row_stride, int Di, int idx_dtype,
+                                         int kv_fp8, const PackLayers& layers, int n_layers, cudaStream_t s);
 cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r,
                                   const float* gamma, float eps, float rope_base,
                                   const int32_t* first_entry, const int32_t* n_rows,

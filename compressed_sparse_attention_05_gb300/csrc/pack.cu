@@ -180,21 +180,18 @@ __device__ __forceinline__ void load_latent(const LatentSource& src, int64_t m, 
 }
 
 // RMSNorm + RoPE (at the entry position 4e + 3) + MXFP4 pack + paged store of
-// one entry per warp.  Lane l owns channels 16l .. 16l+15 (one MXFP4 group).
-__global__ void __launch_bounds__(kNrpWarps * 32)
-k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
-                 float eps, float rope_base, const int32_t* __restrict__ first_entry,
-                 const int32_t* __restrict__ n_rows, const int32_t* __restrict__ page_table,
-                 int max_pages, int64_t n_pages, uint8_t* __restrict__ kv_codes,
-                 uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
-                 int Di, int idx_dtype, void* idx_k, int kv_fp8, const __grid_constant__ RopeTurns rope,
-                 uint32_t* status) {
-  __shared__ __align__(16) float row_buf[kNrpWarps][512];
-  pdl_trigger();
-  pdl_wait();
-  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
-  if (m >= (int64_t)B * n_max) return;
+// entry m (sequence m / n_max, its entry m % n_max), one warp.  Lane l owns
+// channels 16l .. 16l+15 (one MXFP4 group).
+__device__ __forceinline__ void norm_rope_pack_entry(const LatentSource& src, int64_t m, int n_max, int d, int r,
+                                                     const float* __restrict__ gamma, float eps,
+                                                     const int32_t* __restrict__ first_entry,
+                                                     const int32_t* __restrict__ n_rows,
+                                                     const int32_t* __restrict__ page_table, int max_pages,
+                                                     int64_t n_pages, uint8_t* __restrict__ kv_codes,
+                                                     uint8_t* __restrict__ kv_scales, const float* idx_src,
+                                                     int64_t idx_row_stride, int Di, int idx_dtype, void* idx_k,
+                                                     int kv_fp8, const RopeTurns& rope, float* row, int lane,
+                                                     uint32_t* status) {
   const int b = (int)(m / n_max), i = (int)(m % n_max);
   if (n_rows && i >= n_rows[b]) return;
   const int e = first_entry[b] + i;
@@ -204,10 +201,10 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
   const bool has = lane < d / 16;
   float v[16];
   load_latent(src, m, has, lane, v);
-  norm_rope_row(v, has, d, r, gamma, eps, 4ull * (uint64_t)e + 3ull, rope, row_buf[warp], lane);
+  norm_rope_row(v, has, d, r, gamma, eps, 4ull * (uint64_t)e + 3ull, rope, row, lane);
   if (kv_fp8) {   // the FP8 main-KV format: R5's row rule, one fp32 scale per entry
     __syncwarp();
-    fp8_row(row_buf[warp], d, kv_codes + slot * d, reinterpret_cast<float*>(kv_scales) + slot, lane);
+    fp8_row(row, d, kv_codes + slot * d, reinterpret_cast<float*>(kv_scales) + slot, lane);
   } else if (has) {
     Mxfp4Group g = pack_group16(v);
     reinterpret_cast<uint2*>(kv_codes + slot * (d / 2))[lane] = g.codes;
@@ -225,6 +222,49 @@ k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* 
         reinterpret_cast<float*>(idx_k)[slot * Di + c] = acc;
     }
   }
+}
+
+__global__ void __launch_bounds__(kNrpWarps * 32)
+k_norm_rope_pack(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
+                 float eps, const int32_t* __restrict__ first_entry,
+                 const int32_t* __restrict__ n_rows, const int32_t* __restrict__ page_table,
+                 int max_pages, int64_t n_pages, uint8_t* __restrict__ kv_codes,
+                 uint8_t* __restrict__ kv_scales, const float* idx_src, int64_t idx_row_stride,
+                 int Di, int idx_dtype, void* idx_k, int kv_fp8, const __grid_constant__ RopeTurns rope,
+                 uint32_t* status) {
+  __shared__ __align__(16) float row_buf[kNrpWarps][512];
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
+  if (m >= (int64_t)B * n_max) return;
+  norm_rope_pack_entry(src, m, n_max, d, r, gamma, eps, first_entry, n_rows, page_table, max_pages, n_pages, kv_codes,
+                       kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, kv_fp8, rope, row_buf[warp], lane,
+                       status);
+}
+
+// The same for several layers at once (grid.y = layer): every layer's latent
+// and index-key columns lie at a fixed stride in one GEMM output, its gamma at
+// a fixed stride, and its cache where its own pointers say.
+__global__ void __launch_bounds__(kNrpWarps * 32)
+k_norm_rope_pack_layers(LatentSource src, int B, int n_max, int d, int r, const float* __restrict__ gamma,
+                        float eps, const int32_t* __restrict__ first_entry, int max_pages, const float* idx_src,
+                        int64_t idx_row_stride, int Di, int idx_dtype, int kv_fp8,
+                        const __grid_constant__ PackLayers layers, const __grid_constant__ RopeTurns rope,
+                        uint32_t* status) {
+  __shared__ __align__(16) float row_buf[kNrpWarps][512];
+  pdl_trigger();
+  pdl_wait();
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int64_t m = (int64_t)blockIdx.x * kNrpWarps + warp;
+  if (m >= (int64_t)B * n_max) return;
+  const int l = (int)blockIdx.y;
+  const PackLayer& c = layers.l[l];
+  LatentSource ls = src;
+  ls.base += l * layers.col_stride;
+  norm_rope_pack_entry(ls, m, n_max, d, r, gamma + l * layers.gamma_stride, eps, first_entry, nullptr, c.page_table,
+                       max_pages, c.n_pages, c.kv_codes, c.kv_scales, idx_src ? idx_src + l * layers.col_stride : nullptr,
+                       idx_row_stride, Di, idx_dtype, c.idx_k, kv_fp8, rope, row_buf[warp], lane, status);
 }
 
 // Window rows of replayed tokens (SWA Bounded Replay, reading R13): one warp
@@ -318,8 +358,21 @@ cudaError_t launch_norm_rope_pack(LatentSource src, int B, int n_max, int d, int
   if (r < 0 || r / 2 > 256 || (kv_fp8 && d != 512)) return cudaErrorInvalidValue;
   const RopeTurns rope = rope_turns(r, rope_base);
   return launch_step(k_norm_rope_pack, dim3(grid_for(rows, kNrpWarps)), dim3(kNrpWarps * 32), 0, s,
-      src, B, n_max, d, r, gamma, eps, rope_base, first_entry, n_rows, page_table, max_pages,
+      src, B, n_max, d, r, gamma, eps, first_entry, n_rows, page_table, max_pages,
       n_pages, kv_codes, kv_scales, idx_src, idx_row_stride, Di, idx_dtype, idx_k, kv_fp8, rope, status_word());
+}
+
+cudaError_t launch_norm_rope_pack_layers(LatentSource src, int B, int n_max, int d, int r, const float* gamma,
+                                         float eps, float rope_base, const int32_t* first_entry, int max_pages,
+                                         const float* idx_src, int64_t idx_row_stride, int Di, int idx_dtype,
+                                         int kv_fp8, const PackLayers& layers, int n_layers, cudaStream_t s) {
+  const int64_t rows = (int64_t)B * n_max;
+  if (rows == 0 || n_layers == 0) return cudaSuccess;
+  if (r < 0 || r / 2 > 256 || (kv_fp8 && d != 512) || n_layers > kPackLayersMax) return cudaErrorInvalidValue;
+  const RopeTurns rope = rope_turns(r, rope_base);
+  return launch_step(k_norm_rope_pack_layers, dim3(grid_for(rows, kNrpWarps), (unsigned)n_layers),
+                     dim3(kNrpWarps * 32), 0, s, src, B, n_max, d, r, gamma, eps, first_entry, max_pages, idx_src,
+                     idx_row_stride, Di, idx_dtype, kv_fp8, layers, rope, status_word());
 }
 
 cudaError_t launch_norm_rope_fp8_window(LatentSource src, int B, int n_tok, int d, int r,
