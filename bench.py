@@ -365,7 +365,7 @@ def ced_setup(dev):
 
 def run_ced(args, rank, world, dist):
     """--workload ced_compress: one step = CED_LAYERS layers' KV of the prefill chunk
-    from one hidden state (one GEMM over the stacked weights, per-layer pack)."""
+    from one hidden state (one GEMM over the stacked weights, then every layer's pack in one launch)."""
     import torch
 
     from compressed_sparse_attention_05_gb300 import abi, build
@@ -430,7 +430,7 @@ def run_ced(args, rank, world, dist):
                    "tokens_per_step": wl.n_new, "layers": CED_LAYERS, "d": wl.d, "Di": wl.Di,
                    "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "tensor", "kernel": "k_compress_gemm_tma (+ k_norm_rope_pack per layer)",
+        "roofline": {"bound": "tensor", "kernel": "k_compress_gemm_tma (+ k_norm_rope_pack_layers)",
                      "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": None, "algorithmic_flops_per_launch": flops,
                      "kernel_ms": ms, "peak_source": peaks["source"] + " (bf16 burst)"},
