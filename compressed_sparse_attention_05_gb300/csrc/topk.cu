@@ -1387,8 +1387,11 @@ cudaError_t launch_topk(const float* scores, int64_t rows, int64_t stride, Valid
     return launch_step(k_topk_short<false>, dim3((unsigned)rows), dim3(kShortThreads), ssm, s, scores, stride, v, k,
                        out_idx, out_cnt, remap);
   }
-  if (hist && rows * kTopkRanks <= sms && span <= kClusterMaxN && span > kTopkThreads * 8) {
-    // a cluster per row (few rows with a histogram: decode)
+  if (hist && rows * kTopkRanks <= sms && span <= kClusterMaxN && span > kTopkThreads * 8 &&
+      k <= kClusterCap / kTopkRanks) {
+    // a cluster per row (few rows with a histogram, K <= 512: decode).  A larger K (the block
+    // pool's 2,048 blocks) crowds the threshold bin past the cluster's candidate store, and
+    // one CTA per row (k_topk_hist, below) is faster there: 29 against 55 us for 8 rows.
     const bool vec = (reinterpret_cast<uintptr_t>(scores) & 15) == 0 && stride % 4 == 0;
     const size_t csm = sizeof(TopkClusterSmem);
     auto kern = vec ? k_topk_cluster<true> : k_topk_cluster<false>;

@@ -194,7 +194,8 @@ def test_topk_bit_exact_rows_in_registers(stride, k):
 @pytest.mark.parametrize("k", [512, 2048])
 def test_topk_bit_exact_with_histogram(stride, k):
     """Row histograms given (the workspace path builds them first): rows of
-    8,193..32,768 entries are spread over a cluster of CTAs per row."""
+    8,193..32,768 entries are spread over a cluster of CTAs per row for K = 512
+    and taken by one CTA per row for K = 2,048."""
     s, nv = _score_rows()
     s = s[:, :stride].contiguous() if stride <= s.shape[1] else torch.nn.functional.pad(
         s, (0, stride - s.shape[1]), value=float("nan")).contiguous()
