@@ -426,7 +426,8 @@ def run_ced(args, rank, world, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"ced_compress_{CED_LAYERS}layers_chunk{wl.n_new}",
                    "description": f"{CED_LAYERS} layers' KV of a {wl.n_new}-token chunk (hidden {wl.H}) from one "
-                                  "hidden state: one GEMM over the stacked weights, per-layer RMSNorm/RoPE/MXFP4",
+                                  "hidden state: one GEMM over the stacked weights, then every layer's RMSNorm/RoPE/MXFP4 "
+                                  "in one launch",
                    "tokens_per_step": wl.n_new, "layers": CED_LAYERS, "d": wl.d, "Di": wl.Di,
                    "l2": "flushed before every timed step (512 MB written, then 512 MB read)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
