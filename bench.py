@@ -397,21 +397,47 @@ def run_ced(args, rank, world, dist):
     launches = abi.csa2_launch_count() - n0
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(sum(step_ms) / args.steps, dist, dev)
-    # end to end: the chunk's hidden states in from pinned host memory, the last layer's codes back
+    # end to end, as a serving loop runs it: the chunk's hidden states in from pinned host
+    # memory and the last layer's codes back, two buffer sets (hidden state and caches),
+    # uploads and downloads on two copy streams overlapping each other and the steps
+    sets = [(hidden, keep, step), ced_setup(dev)[1:]]
     h_in = hidden.cpu().pin_memory()
-    h_out = torch.empty(keep[-1]["codes"].shape, dtype=torch.uint8, pin_memory=True)
+    h_out = [torch.empty(keep[-1]["codes"].shape, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    cs_up, cs_dn = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def e2e_run(n_steps):
+        up = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        down = [torch.cuda.Event() for _ in range(2)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(cs_up)
+        cs_dn.wait_event(t0)
+        for i in range(n_steps + 2):
+            j = i % 2
+            hid, kp, st = sets[j]
+            if i >= 2:   # set j: step i-2 has finished; its last layer's codes go to the host
+                with torch.cuda.stream(cs_dn):
+                    cs_dn.wait_event(done[j])
+                    h_out[j].copy_(kp[-1]["codes"], non_blocking=True)
+                    down[j].record(cs_dn)
+            if i < n_steps:
+                with torch.cuda.stream(cs_up):
+                    if i >= 2:
+                        cs_up.wait_event(done[j])
+                    hid.copy_(h_in, non_blocking=True)
+                    up[j].record(cs_up)
+                stream.wait_event(up[j])
+                if i >= 2:
+                    stream.wait_event(down[j])
+                st()
+                done[j].record(stream)
+        t1.record(cs_dn)
+        t1.synchronize()
+        return t0.elapsed_time(t1)
+
+    e2e_run(3)   # warm-up
     n = max(3, min(args.steps, 50))
-    tot = 0.0
-    for k in range(n):
-        flush(k)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        hidden.copy_(h_in, non_blocking=True)
-        step()
-        h_out.copy_(keep[-1]["codes"], non_blocking=True)
-        b.record(stream)
-        b.synchronize()
-        tot += a.elapsed_time(b)
+    tot = e2e_run(n)
     e2e_ms = max_over_ranks(tot / n, dist, dev)
     status = abi.csa2_get_status()
     if rank != 0:
@@ -436,7 +462,9 @@ def run_ced(args, rank, world, dist):
                      "frac": achieved / peaks["bf16_tflops"], "traffic": None, "algorithmic_flops_per_launch": flops,
                      "kernel_ms": ms, "peak_source": peaks["source"] + " (bf16 burst)"},
         "e2e": {"value": world * wl.n_new / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": hidden.numel() * 2, "d2h_bytes_per_step": h_out.numel()},
+                "h2d_bytes_per_step": hidden.numel() * 2, "d2h_bytes_per_step": h_out[0].numel(),
+                "pipeline": "two buffer sets (hidden state and caches); uploads and downloads on two copy "
+                            "streams overlap each other and the steps; no L2 flush"},
         "gpu_launches": launches, "status_word": status,
         "step_ms_p50": statistics.median(step_ms), "step_ms_min": min(step_ms), "clocks": clk.summary(),
     }
