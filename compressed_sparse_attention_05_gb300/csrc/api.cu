@@ -636,8 +636,18 @@ static int index_topk_impl(const csa2_dims* dm, const csa2_cache* c, const void*
              "block_pool");
     }
   } else {
-    LAUNCH(launch_index_scores_pool(a, pool, pool_cnt, dm->n_pool_blocks, 8, scores, L.s_stride, nvalid, s),
-           "index_scores_pool");
+    const int64_t pool_pos = (int64_t)dm->n_pool_blocks * 8;
+    if (index_scores_gemm_supported(a) && max_entries > 0 && 4 * pool_pos >= max_entries) {
+      // many query tokens over a pool that covers a good share of the entries: score
+      // every visible entry on the tensor cores (the same score per position, R10),
+      // then keep the pooled positions' scores
+      LAUNCH(launch_index_scores_gemm(a, scores, L.s_stride, nullptr, 0, max_entries, s), "index_scores_gemm");
+      LAUNCH(launch_pool_compact(a, pool, pool_cnt, dm->n_pool_blocks, scores, L.s_stride, nvalid, s),
+             "pool_compact");
+    } else {
+      LAUNCH(launch_index_scores_pool(a, pool, pool_cnt, dm->n_pool_blocks, 8, scores, L.s_stride, nvalid, s),
+             "index_scores_pool");
+    }
     ValidSpec v{nvalid, nullptr, nullptr, 1, 1, 0};
     LAUNCH(launch_topk(scores, rows, L.s_stride, v, dm->K, out_idx, out_cnt,
                        Remap{pool, dm->n_pool_blocks, 8}, nullptr, 0, s, (int64_t)dm->n_pool_blocks * 8),

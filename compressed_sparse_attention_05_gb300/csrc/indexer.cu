@@ -565,6 +565,66 @@ k_index_scores_pool_mma(IndexerArgs a, const int32_t* __restrict__ pool,
   if (t == 1 && vg8) scores[row * stride + 8 * (p0 + 1) + g] = s1;
 }
 
+// Reindex over many query tokens: the pooled positions' scores gathered from a
+// row of scores of every visible entry (the tensor-core GEMM's output) into
+// compact columns 8*slot + e of the same row, with the pool scorer's count of
+// visible positions and its check of the pool.  One CTA per row; every value
+// is read before any is written, so the pool's order does not matter.
+constexpr int kCompactThreads = 1024;
+constexpr int kCompactPer = 32;   // 8 x 4,096 pooled positions at most
+__global__ void __launch_bounds__(kCompactThreads, 1)
+k_pool_compact(IndexerArgs a, const int32_t* __restrict__ pool, const int32_t* __restrict__ pool_cnt, int n_pool,
+               float* __restrict__ scores, int64_t stride, int32_t* __restrict__ n_valid, uint32_t* status) {
+  __shared__ int s_cnt[kCompactThreads / 32];
+  pdl_trigger();
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  const int b = (int)(row / a.Tq);
+  const int nv = n_visible(min(a.n_entries[b], a.max_entries), a.q_pos[row]);
+  const int pc = min(max(pool_cnt[row], 0), n_pool);
+  const int32_t* prow = pool + row * n_pool;
+  float* srow = scores + row * stride;
+  const int tid = threadIdx.x;
+  float v[kCompactPer];
+  uint32_t keep = 0;   // bit k: value k is written back
+  int cnt = 0;
+#pragma unroll
+  for (int k = 0; k < kCompactPer; ++k) {
+    const int c = tid + kCompactThreads * k;
+    v[k] = 0.f;
+    if (c < 8 * pc) {
+      const int32_t blk = prow[c >> 3];
+      const int64_t e = 8LL * blk + (c & 7);
+      if (blk >= 0 && e < nv) {
+        v[k] = srow[e];
+        keep |= 1u << k;
+      }
+      cnt += (c & 7) < visible_in_block(nv, blk) ? 1 : 0;
+      if ((c & 7) == 0 && (blk < 0 || 8LL * blk >= nv)) raise_status(status, CSA2_STATUS_BAD_INDEX);
+    }
+  }
+  cnt = (int)warp_sum((float)cnt);
+  if ((tid & 31) == 0) s_cnt[tid >> 5] = cnt;
+  __syncthreads();   // (also: every read of the row is done before the writes below)
+  if (tid < 32) {
+    int t = s_cnt[tid];
+    t = (int)warp_sum((float)t);
+    if (tid == 0) n_valid[row] = t;
+  }
+#pragma unroll
+  for (int k = 0; k < kCompactPer; ++k)
+    if ((keep >> k) & 1u) srow[tid + kCompactThreads * k] = v[k];
+}
+
+cudaError_t launch_pool_compact(const IndexerArgs& a, const int32_t* pool, const int32_t* pool_cnt, int n_pool,
+                                float* scores, int64_t stride, int32_t* n_valid, cudaStream_t s) {
+  const int64_t rows = (int64_t)a.B * a.Tq;
+  if (rows == 0) return cudaSuccess;
+  if (n_pool > kCompactThreads * kCompactPer / 8) return cudaErrorInvalidValue;
+  return launch_step(k_pool_compact, dim3((unsigned)rows), dim3(kCompactThreads), 0, s, a, pool, pool_cnt, n_pool,
+                     scores, stride, n_valid, status_word());
+}
+
 // Generic path (fp32 keys, or shapes the tensor-core path does not take):
 // one thread per (query, entry), query staged in shared memory.
 template <typename T>

@@ -139,6 +139,10 @@ cudaError_t launch_index_scores(const IndexerArgs& a, float* scores, int64_t str
 // ---- indexer_tc.cu: many query tokens per sequence (prefill) as a tcgen05 GEMM
 // (bf16 keys, Hi = 8, Di = 128, Tq >= 32).  Scores and block maxima as above;
 // builds no histogram (the Top-K kernel builds its own).
+// Reindex from full score rows: the pooled positions' scores gathered into compact
+// columns 8*slot + e of the same rows (in place), and the visible count per row.
+cudaError_t launch_pool_compact(const IndexerArgs& a, const int32_t* pool, const int32_t* pool_cnt, int n_pool,
+                                float* scores, int64_t stride, int32_t* n_valid, cudaStream_t s);
 bool index_scores_gemm_supported(const IndexerArgs& a);
 cudaError_t launch_index_scores_gemm(const IndexerArgs& a, float* scores, int64_t stride, float* blockmax,
                                      int64_t bm_stride, int max_entries, cudaStream_t s);
