@@ -23,20 +23,24 @@ def _np(t):
     return t.detach().cpu().double().numpy()
 
 
-@pytest.mark.parametrize("d,r,Di,idx_dtype,kv,G", [(512, 64, 128, "bf16", "mxfp4", 70), (512, 64, 0, "bf16", "mxfp4", 70),
-                                                  (64, 16, 32, "f32", "mxfp4", 70), (512, 64, 128, "bf16", "fp8", 70),
-                                                  (512, 64, 128, "bf16", "mxfp4", 256),
-                                                  (512, 64, 128, "bf16", "mxfp4", 507),
-                                                  (512, 64, 0, "bf16", "mxfp4", 507)])
-def test_compress_layers_matches_oracle(d, r, Di, idx_dtype, kv, G):
+@pytest.mark.parametrize("d,r,Di,idx_dtype,kv,G,L", [(512, 64, 128, "bf16", "mxfp4", 70, 3),
+                                                    (512, 64, 0, "bf16", "mxfp4", 70, 3),
+                                                    (64, 16, 32, "f32", "mxfp4", 70, 3),
+                                                    (512, 64, 128, "bf16", "fp8", 70, 3),
+                                                    (512, 64, 128, "bf16", "mxfp4", 256, 3),
+                                                    (512, 64, 128, "bf16", "mxfp4", 507, 3),
+                                                    (512, 64, 0, "bf16", "mxfp4", 507, 3),
+                                                    (512, 64, 128, "bf16", "mxfp4", 70, 66)])
+def test_compress_layers_matches_oracle(d, r, Di, idx_dtype, kv, G, L):
     """kv = "fp8": the V4-style main KV (E4M3 row + fp32 scale per entry).  G entries
     per sequence: 70 (one M tile), 256 (two: CTA pairs share each weight tile) and
     507 (four, the last ragged: clusters of four share it, the index-key tile's
-    rows copied by two of them)."""
+    rows copied by two of them).  L = 66 layers: the per-layer packs run 64 layers
+    per launch, so the last two go in a second launch."""
     fp8 = kv == "fp8"
     dev = "cuda"
     g = torch.Generator().manual_seed(21)
-    B, H, L = 2, 256, 3
+    B, H = 2, 256
     T = 4 * G + 1                         # G entries per sequence; the last token makes none
     assert T // 4 == G
     first = [10, 0]                       # entries before the new tokens
